@@ -1,0 +1,506 @@
+"""Benchmark of the GB300 GEMM library.
+
+Headline: BF16 NT GEMM at the Qwen-2B-shaped MLP gate/up size
+(M=5120, N=11008, K=2048), TFLOP/s per GPU (whole job over all ranks).  A
+step is one gemm_bf16_nt call (tile scheduler, TMA staging, tcgen05 MMA and
+BF16 epilogue) over one batch of synthetic inputs already resident in HBM.
+Consecutive steps rotate over several copies of the inputs and outputs so
+that the working set (> 2x L2) is never served from L2.  The other shapes of
+the same metric (down, qkv, gqa, the LoRA fold, the router and the NVFP4
+GEMM) are measured the same way and reported under "shapes".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense BF16/FP4 tensor peak, per shape"
+L2_BYTES = 129 * 1024 * 1024
+FP4_PEAK_RATIO = 6.0  # nominal dense FP4 / dense BF16 tensor rate on GB300 (13.5 / 2.25)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-shapes", action="store_true", help="headline shape only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--clock-warm-s", type=float, default=0.6,
+                    help="extra warm-up seconds so that clock samples cover the load")
+    ap.add_argument("--shapes", default="down,qkv,gqa,lora,router,nvfp4",
+                    help="comma list of the extra shapes to measure")
+    ap.add_argument("--no-headline", action="store_true",
+                    help="profiling aid: measure only --shapes and print them")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampler running while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [p for (t, p) in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        smax = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        power = [num(p[3]) for p in win if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "power_w_max": max(power) if power else None, "samples": len(win)}
+
+
+# ----------------------------------------------------------------- timing
+def time_launches(torch, stream, fn, n_sets, warmup, steps, min_warm_s=0.0):
+    """Run `fn(i % n_sets)` warmup + steps times on `stream`; time the steps
+    with CUDA events recorded on that stream.  Returns (seconds per step,
+    wall-clock window of the timed region)."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i % n_sets)
+        stream.synchronize()
+        if min_warm_s > 0:  # keep the GPU busy long enough for clock samples
+            t_end = time.time() + min_warm_s
+            i = 0
+            while time.time() < t_end:
+                for _ in range(20):
+                    fn(i % n_sets)
+                    i += 1
+                stream.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        start.record(stream)
+        for i in range(steps):
+            fn(i % n_sets)
+        end.record(stream)
+        end.synchronize()
+        t1 = time.time()
+    return start.elapsed_time(end) / 1e3 / steps, (t0, t1)
+
+
+def n_sets_for(bytes_per_set: int) -> int:
+    return max(2, -(-2 * L2_BYTES // max(1, bytes_per_set)) + 1)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_tcgen05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_baseline(seconds: float):
+    """The oracle, as it stands, on whole sampled rows of the gate/up GEMM."""
+    import oracle
+    from nvfp4_block_scaled_tcgen05_gb300 import synth
+    w = synth.BF16_WORKLOADS["gateup"]
+    A, B = synth.gemm_inputs(w)
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(0)
+    rows_done, t_spent, chunk = 0, 0.0, max(threads, 16)
+    while t_spent < seconds and rows_done < w.M:
+        rows = rng.integers(0, w.M, size=chunk)
+        t0 = time.perf_counter()
+        oracle.gemm_bf16_nt(A, B, rows=rows, threads=threads)
+        t_spent += time.perf_counter() - t0
+        rows_done += chunk
+        chunk = min(chunk * 2, 4 * threads * 8)
+    flops = 2.0 * rows_done * w.N * w.K
+    return {"value": flops / t_spent / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{rows_done} sampled rows of the 5120x11008x2048 BF16 GEMM "
+                      f"({flops / 1e9:.1f} GFLOP in {t_spent:.1f} s)"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, timed as it stands on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from nvfp4_block_scaled_tcgen05_gb300 import synth
+    w = synth.BF16_WORKLOADS["gateup"]
+    A, B = synth.gemm_inputs(w)
+    threads = oracle.default_threads()
+    rows_per_step = 4 * threads
+    rng = np.random.default_rng(1)
+    for _ in range(args.warmup):
+        oracle.gemm_bf16_nt(A, B, rows=rng.integers(0, w.M, rows_per_step), threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_bf16_nt(A, B, rows=rng.integers(0, w.M, rows_per_step), threads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows_per_step * w.N * w.K / dt / 1e12
+    sample = f"{rows_per_step} sampled rows of the 5120x11008x2048 BF16 GEMM per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "bf16 NT GEMM M=5120 N=11008 K=2048 (MLP gate/up), row sample"},
+        "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value,
+                         "unit": "TFLOP/s"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+# ----------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import nvfp4_block_scaled_tcgen05_gb300 as g
+    from nvfp4_block_scaled_tcgen05_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    __graft_entry__.build()
+    lib = g.load()
+    pk = peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def up(x, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.to(dev)
+
+    if args.no_headline:
+        shapes = measure_shapes(torch, lib, synth, up, stream, dev, pk, max(3, args.warmup),
+                                args.steps, args.shapes.split(","))
+        if rank == 0:
+            print(json.dumps({"shapes": shapes}))
+        return
+
+    # ------------------------------------------------ headline: gate/up
+    w = synth.BF16_WORKLOADS["gateup"]
+    A_h, B_h = synth.gemm_inputs(w, seed_offset=rank)
+    set_bytes = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
+    nsets = n_sets_for(set_bytes)
+    A0, B0 = up(A_h, torch.bfloat16), up(B_h, torch.bfloat16)
+    As = [A0] + [A0.clone() for _ in range(nsets - 1)]
+    Bs = [B0] + [B0.clone() for _ in range(nsets - 1)]
+    Cs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(nsets)]
+    sp = stream.cuda_stream
+
+    def step(i):
+        rc = lib.gemm_bf16_nt(As[i].data_ptr(), Bs[i].data_ptr(), Cs[i].data_ptr(), w.M, w.N, w.K, sp)
+        if rc:
+            raise RuntimeError(g.status_string(rc))
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    t_load0 = time.time()
+    sec, (t0, t1) = time_launches(torch, stream, step, nsets, max(3, args.warmup), args.steps,
+                                  min_warm_s=args.clock_warm_s)
+    barrier()
+    clocks.stop()
+    clk = clocks.summary(t_load0, t1)
+    sec = max_over_ranks(sec)
+    flops = 2.0 * w.M * w.N * w.K
+    per_gpu_tflops = flops / sec / 1e12
+    value = world * per_gpu_tflops
+    assert lib.gemm_get_device_status(sp) == 0
+
+    # ------------------------------------------------ e2e through host buffers
+    A_pin = torch.from_numpy(A_h.view(np.int16)).pin_memory()
+    B_pin = torch.from_numpy(B_h.view(np.int16)).pin_memory()
+    C_pin = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+    A_u16, B_u16 = As[0].view(torch.int16), Bs[0].view(torch.int16)
+    C_u16 = Cs[0].view(torch.int16)
+
+    def e2e_step(_):
+        A_u16.copy_(A_pin, non_blocking=True)
+        B_u16.copy_(B_pin, non_blocking=True)
+        step(0)
+        C_pin.copy_(C_u16, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_sec, _ = time_launches(torch, stream, e2e_step, 1, 2, e2e_steps)
+    e2e_sec = max_over_ranks(e2e_sec)
+    h2d = (w.M * w.K + w.N * w.K) * 2
+    d2h = w.M * w.N * 2
+    # the e2e output must equal the device-resident result bit for bit
+    e2e_ok = bool(torch.equal(C_pin.to(dev), Cs[0].view(torch.int16)))
+
+    del As, Bs, Cs
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------ other shapes
+    shapes = []
+    if not args.no_shapes:
+        shapes = measure_shapes(torch, lib, synth, up, stream, dev, pk, max(3, args.warmup),
+                                30, args.shapes.split(","))
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "bf16 NT GEMM M=5120 N=11008 K=2048 (Qwen-2B-shaped MLP gate/up)",
+                   "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}",
+                   "l2": f"rotating {nsets} input/output sets ({nsets * set_bytes / 2**20:.0f} MiB "
+                         f"> 2x L2) between steps"},
+        "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": per_gpu_tflops / pk["bf16_tflops"],
+                     "peak_source": f"{pk['source']} cuBLAS bf16 burst",
+                     "kernel": "tcgen05_gemm_kernel<bf16,256,4,StoreBF16>",
+                     "traffic": recorded_traffic("gemm_bf16_gateup")},
+        "e2e": {"value": world * flops / e2e_sec / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_sec * 1e3, "matches_device_result": e2e_ok},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "shapes": shapes,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
+    sp = stream.cuda_stream
+    which = {w.strip() for w in which if w.strip()}
+    out = []
+    bf16_peak = pk["bf16_tflops"]
+    fp4_peak = bf16_peak * FP4_PEAK_RATIO
+
+    def check(rc):
+        if rc:
+            raise RuntimeError(f"status {rc}")
+
+    # plain BF16 shapes
+    for name in ("down", "qkv", "gqa", "gateup"):
+        if name not in which:
+            continue
+        w = synth.BF16_WORKLOADS[name]
+        A_h, B_h = synth.gemm_inputs(w)
+        set_bytes = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
+        n = n_sets_for(set_bytes)
+        A0, B0 = up(A_h, torch.bfloat16), up(B_h, torch.bfloat16)
+        As = [A0] + [A0.clone() for _ in range(n - 1)]
+        Bs = [B0] + [B0.clone() for _ in range(n - 1)]
+        Cs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        fn = lambda i: check(lib.gemm_bf16_nt(As[i].data_ptr(), Bs[i].data_ptr(), Cs[i].data_ptr(),
+                                              w.M, w.N, w.K, sp))
+        sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+        tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+        out.append({"shape": name, "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
+                    "frac_bf16_peak": tf / bf16_peak})
+        del As, Bs, Cs
+
+    if "lora" in which:
+        out.append(measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check))
+    if "router" in which:
+        out.append(measure_router(torch, lib, synth, up, stream, dev, warmup, reps, check))
+    if "nvfp4" in which:
+        out.append(measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_peak))
+    assert lib.gemm_get_device_status(sp) == 0
+    return out
+
+
+def measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check):
+    """LoRA fold: fused scaled-acc vs the unfused pair; HBM-bound."""
+    sp = stream.cuda_stream
+    w = synth.LORA
+    X_h, W_h = synth.gemm_inputs(w)
+    O_h = synth.scaled_acc_out(w.M, w.N, w.seed)
+    Xd, Wd = up(X_h, torch.bfloat16), up(W_h, torch.bfloat16)
+    n = n_sets_for(w.M * w.N * 2)
+    Os = [up(O_h, torch.bfloat16) for _ in range(n)]
+    scratch = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    import ctypes
+    sc = ctypes.c_float(synth.LORA_SCALE)
+    fused = lambda i: check(lib.gemm_bf16_nt_scaled_acc(Xd.data_ptr(), Wd.data_ptr(), Os[i].data_ptr(),
+                                                        w.M, w.N, w.K, sc, sp))
+    def unfused(i):
+        check(lib.gemm_bf16_nt(Xd.data_ptr(), Wd.data_ptr(), scratch.data_ptr(), w.M, w.N, w.K, sp))
+        check(lib.bf16_scaled_add(Os[i].data_ptr(), scratch.data_ptr(), sc, w.M * w.N, sp))
+    sec_f, _ = time_launches(torch, stream, fused, n, warmup, reps)
+    sec_u, _ = time_launches(torch, stream, unfused, n, warmup, reps)
+    bytes_fused = 2 * w.M * w.N * 2 + (w.M + w.N) * w.K * 2
+    res = {"shape": "lora_fold", "M": w.M, "N": w.N, "K": w.K, "us": sec_f * 1e6,
+           "GB/s": bytes_fused / sec_f / 1e9,
+           "frac_hbm_peak": bytes_fused / sec_f / 1e9 / pk["hbm_gbs"],
+           "unfused_us": sec_u * 1e6, "fused_speedup": sec_u / sec_f,
+           "TFLOP/s": 2.0 * w.M * w.N * w.K / sec_f / 1e12}
+    del Os, scratch
+    return res
+
+
+def measure_router(torch, lib, synth, up, stream, dev, warmup, reps, check):
+    """Ordered router GEMM on CUDA cores (no-FMA FP32: 1 flop per lane per clock)."""
+    sp = stream.cuda_stream
+    w = synth.ROUTER
+    A_h, B_h = synth.gemm_inputs(w)
+    n = n_sets_for((w.M * w.K + w.N * w.K) * 2 + w.M * w.N * 4)
+    A0, B0 = up(A_h, torch.bfloat16), up(B_h, torch.bfloat16)
+    Ad = [A0] + [A0.clone() for _ in range(n - 1)]
+    Bd = [B0] + [B0.clone() for _ in range(n - 1)]
+    Cr = [torch.empty((w.M, w.N), dtype=torch.float32, device=dev) for _ in range(n)]
+    fn = lambda i: check(lib.gemm_bf16_nt_ordered(Ad[i].data_ptr(), Bd[i].data_ptr(),
+                                                  Cr[i].data_ptr(), w.M, w.N, w.K, sp))
+    sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    props = torch.cuda.get_device_properties(dev)
+    alu_peak = props.multi_processor_count * 128 * 2070e6 / 1e12  # TFLOP/s at max SM clock
+    tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+    res = {"shape": "router", "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
+           "frac_alu_peak": tf / alu_peak, "alu_peak_tflops": alu_peak}
+    del Ad, Bd, Cr
+    return res
+
+
+def measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_peak):
+    """NVFP4 block-scaled GEMM at L=1, 4096 x 7168 x 16384."""
+    sp = stream.cuda_stream
+    w = synth.NVFP4
+    a_h, b_h, sfa_h, sfb_h = synth.nvfp4_inputs(w)
+    set_bytes = a_h.size + b_h.size + sfa_h.size + sfb_h.size + w.L * w.M * w.N * 2
+    n = n_sets_for(set_bytes)
+    a0, b0, sa0, sb0 = up(a_h), up(b_h), up(sfa_h), up(sfb_h)
+    sets = [(a0, b0, sa0, sb0)] + [(a0.clone(), b0.clone(), sa0.clone(), sb0.clone())
+                                   for _ in range(n - 1)]
+    cs = [torch.empty((w.L, w.M, w.N), dtype=torch.float16, device=dev) for _ in range(n)]
+    fn = lambda i: check(lib.gemm_nvfp4_bs(sets[i][0].data_ptr(), sets[i][1].data_ptr(),
+                                           sets[i][2].data_ptr(), sets[i][3].data_ptr(),
+                                           cs[i].data_ptr(), w.L, w.M, w.N, w.K, sp))
+    sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    tf = 2.0 * w.L * w.M * w.N * w.K / sec / 1e12
+    res = {"shape": "nvfp4", "L": w.L, "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6,
+           "TFLOP/s": tf, "frac_fp4_peak": tf / fp4_peak, "fp4_peak_tflops": fp4_peak,
+           "fp4_peak_source": "measured bf16 burst x nominal fp4/bf16 ratio 6"}
+    del sets, cs
+    return res
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * gb300gemm.h - C ABI of the GB300 (sm_103a) dense NT GEMM library.
+ *
+ * All entry points:
+ *  - take plain pointers and sizes; no framework types cross this boundary;
+ *  - take DEVICE pointers for every matrix (memory the caller allocated on
+ *    the current CUDA device); the library allocates no per-call memory and
+ *    never takes ownership of a buffer;
+ *  - enqueue their work on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and return without synchronising;
+ *  - validate every argument on the host BEFORE launching anything and
+ *    return a GEMM_ERR_* code without side effects when validation fails;
+ *  - return GEMM_OK (0) when the work was enqueued.
+ *
+ * Device-side wait limits: every wait inside a kernel is bounded (about two
+ * seconds).  A kernel that runs out of a wait stops, records a code in a
+ * device status word and returns; gemm_get_device_status() reports it.
+ *
+ * Layouts are row-major.  "NT" means C[M,N] = A[M,K] . B[N,K]^T, i.e. B is
+ * stored like a HuggingFace weight ([out_features, in_features]).
+ */
+#ifndef GB300GEMM_H
+#define GB300GEMM_H
+
+#if defined(__GNUC__)
+#define GB300GEMM_API __attribute__((visibility("default")))
+#else
+#define GB300GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define GEMM_OK             0
+#define GEMM_ERR_NULL       1  /* a required pointer is NULL */
+#define GEMM_ERR_SHAPE      2  /* a dimension is <= 0, too large, or breaks a multiple-of rule */
+#define GEMM_ERR_ALIGN      3  /* a pointer or a row pitch is not 16-byte aligned */
+#define GEMM_ERR_ALIAS      4  /* an output buffer overlaps an input buffer */
+#define GEMM_ERR_ARCH       5  /* the current device is not an sm_100-family (sm_103) GPU */
+#define GEMM_ERR_LAUNCH     6  /* a CUDA call failed (launch, attribute, tensor-map encode) */
+#define GEMM_ERR_TIMEOUT    7  /* a kernel ran out of a bounded device-side wait */
+#define GEMM_ERR_NO_DEVICE  8  /* no usable CUDA device / driver */
+
+/*
+ * gemm_bf16_nt - dense BF16 GEMM, C = bf16(A . B^T) with FP32 accumulation.
+ *
+ * Defined by: "gemm_dense.rs" (spark_model layers/ops), dense_gemm_tc doc
+ * comment (A [M,K] activations, B [N,K] weights in HuggingFace layout, C
+ * [M,N], all row-major); "sm121a_matmul.py", _sm121a_matmul_kernel (BF16
+ * inputs, FP32 accumulator, BF16 store).
+ *
+ *   A  bf16 [M][K], row pitch K elements     (read)
+ *   B  bf16 [N][K], row pitch K elements     (read)
+ *   C  bf16 [M][N], row pitch N elements     (written; must not overlap A or B)
+ *   M, N, K >= 1;  K % 8 == 0 and N % 8 == 0 (16-byte row pitches);
+ *   A, B, C 16-byte aligned.
+ * The order in which the tensor cores add the K products is the hardware's.
+ * Errors: GEMM_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARCH, _LAUNCH.
+ */
+GB300GEMM_API int gemm_bf16_nt(const void* A, const void* B, void* C, int M, int N, int K, void* stream);
+
+/*
+ * gemm_bf16_nt_scaled_acc - fused LoRA expand+fold:
+ *     C[m,n] = bf16( float(C[m,n]) + scale * float(bf16(sum_k A[m,k] B[n,k])) )
+ * The GEMM result is rounded to BF16 first, then multiplied by `scale` in
+ * FP32, then added in FP32 (separately rounded), then rounded to BF16, so the
+ * result is bit-identical to gemm_bf16_nt into a BF16 scratch followed by
+ * bf16_scaled_add.  C is read once and written once.
+ *
+ * Defined by: "gemm_dense.rs", dense_gemm_tc_scaled_acc doc comment (output
+ * += scale * bf16(input @ weight^T) in one pass, bit-identical to the unfused
+ * GEMM-into-scratch + bf16_scaled_add pair).
+ *
+ *   A, B, M, N, K as for gemm_bf16_nt;  C_inout bf16 [M][N] (read and written
+ *   in place, must not overlap A or B);  scale any finite float.
+ * Errors: as gemm_bf16_nt.
+ */
+GB300GEMM_API int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_inout, int M, int N, int K,
+                            float scale, void* stream);
+
+/*
+ * gemm_bf16_nt_ordered - order-preserving "router" GEMM with FP32 output:
+ *     C[m,n] = (((0 + A[m,0]B[n,0]) + A[m,1]B[n,1]) + ... + A[m,K-1]B[n,K-1])
+ * every product and every sum rounded to FP32 (round to nearest even), no
+ * fused multiply-add, subnormals kept.  Runs on CUDA cores; the result is
+ * bit-identical to the strict sequential loop.
+ *
+ * Defined by: "gemm_dense.rs", dense_gemm_router doc comment (same math and
+ * same per-output FP32 accumulation order, strict k = 0..K-1, as the scalar
+ * dense_gemm; bit-identical under --fmad=false) and dense_gemm.
+ *
+ *   A bf16 [M][K], B bf16 [N][K] (read);  C float [M][N] (written, must not
+ *   overlap A or B);  M, N, K >= 1;  K % 8 == 0;  A, B, C 16-byte aligned.
+ * Errors: GEMM_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _LAUNCH.
+ */
+GB300GEMM_API int gemm_bf16_nt_ordered(const void* A, const void* B, float* C, int M, int N, int K,
+                         void* stream);
+
+/*
+ * gemm_nvfp4_bs - NVFP4 block-scaled GEMM with FP16 output, for each l < L:
+ *     c[l][m][n] = fp16( sum_k  e2m1(a[l][m][k]) * e4m3(SFA(l,m,k/16))
+ *                             * e2m1(b[l][n][k]) * e4m3(SFB(l,n,k/16)) )
+ * accumulated in FP32 on the tensor cores (hardware order).
+ *
+ * Defined by: "kernelbot nvfp4 gemm submission 123329": module docstring
+ * sections "SCALE FACTORS" (one scale per 16 consecutive K elements),
+ * "NVIDIA Block layout" and "Layout semantics" (scale layout below), and
+ * custom_kernel (a, b packed float4_e2m1fn_x2; c float16; mkl -> lmk
+ * physical order; M % 128, N % 128, K % 256 asserts).
+ *
+ *   a    [L][M][K/2] bytes: two e2m1 codes per byte, element 2j in the low
+ *        nibble of byte j and element 2j+1 in the high nibble.
+ *   b    [L][N][K/2] bytes, same packing.
+ *   sfa  L*M*K/16 e4m3 bytes in the hardware layout: logical
+ *        [32,4,M/128,4,K/64,L] with dims [g,i_m,tile,i_k,tile_k,l], row
+ *        r = tile*128 + i_m*32 + g, group j = tile_k*4 + i_k, stored in the
+ *        order l, tile, tile_k, g, i_m, i_k; i.e. the byte of (r, j, l) is at
+ *        ((l*(M/128) + r/128)*(K/64) + j/4)*512 + (r%32)*16 + ((r%128)/32)*4 + j%4.
+ *   sfb  L*N*K/16 bytes, the same layout over N.
+ *   c    fp16 [L][M][N] (written; must not overlap a, b, sfa, sfb).
+ *   L >= 1, M % 128 == 0, N % 128 == 0, K % 256 == 0, all > 0;
+ *   every pointer 16-byte aligned.  Scale bytes are read as unsigned e4m3
+ *   (the sign bit must be clear).
+ * Errors: GEMM_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARCH, _LAUNCH.
+ */
+GB300GEMM_API int gemm_nvfp4_bs(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
+                  int L, int M, int N, int K, void* stream);
+
+/*
+ * bf16_scaled_add - out[i] = bf16( float(out[i]) + scale * float(d[i]) ),
+ * product and sum each rounded to FP32.  The second kernel of the unfused
+ * LoRA pair (GEMM into a BF16 scratch, then this), kept as the baseline the
+ * fused gemm_bf16_nt_scaled_acc must match bit for bit.
+ *
+ * Defined by: "gemm_dense.rs", dense_gemm_tc_scaled_acc doc comment (the
+ * unfused pair: GEMM into scratch, then bf16_scaled_add).
+ *
+ *   out bf16 [n] (read and written), d bf16 [n] (read), n >= 1;
+ *   out and d 16-byte aligned and not overlapping.
+ * Errors: GEMM_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _LAUNCH.
+ */
+GB300GEMM_API int bf16_scaled_add(void* out, const void* d, float scale, long n, void* stream);
+
+/*
+ * gemm_get_device_status - synchronise `stream`, then read and clear the
+ * device status word of the current device.  Returns GEMM_OK, or
+ * GEMM_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, or GEMM_ERR_LAUNCH if the stream reports a CUDA error.
+ * Library extension (the pages define no such call).
+ */
+GB300GEMM_API int gemm_get_device_status(void* stream);
+
+/* gemm_status_string - static, human-readable name of a status code. */
+GB300GEMM_API const char* gemm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300GEMM_H */

@@ -1,0 +1,239 @@
+// C ABI of the library (declared in include/gb300gemm.h): argument
+// validation, per-device state (SM count, status word), TMA descriptor
+// encoding, dispatch to the launchers.  Validation is pure host code and
+// runs before any CUDA call, so a bad call never touches the device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "internal.h"
+
+namespace gb300 {
+
+// Device status word: 0, or 0x100 | where for the first bounded wait that
+// ran out since it was last cleared.
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceSlot {
+  bool ready = false;
+  int rc = GEMM_OK;
+  DeviceInfo info{};
+};
+
+std::mutex g_dev_mutex;
+DeviceSlot g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [a, a+na) and [b, b+nb) overlap?
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+constexpr long long kMaxTiles = 1ll << 30;
+
+}  // namespace
+
+int current_device(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceSlot& s = g_devices[dev];
+  if (!s.ready) {
+    DeviceInfo d{};
+    d.device = dev;
+    int rc = GEMM_OK;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess) {
+      rc = GEMM_ERR_NO_DEVICE;
+    } else if (!(d.cc_major == 10 && d.cc_minor == 3)) {
+      rc = GEMM_ERR_ARCH;  // the library carries sm_103a code only
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word) !=
+               cudaSuccess) {
+      rc = GEMM_ERR_NO_DEVICE;
+    }
+    if (rc != GEMM_OK) cudaGetLastError();
+    s.info = d;
+    s.rc = rc;
+    s.ready = true;
+  }
+  *out = s.info;
+  return s.rc;
+}
+
+unsigned long long wait_timeout_ns() {
+  static unsigned long long ns = [] {
+    const char* e = std::getenv("GB300GEMM_WAIT_TIMEOUT_MS");
+    long ms = e ? std::strtol(e, nullptr, 10) : 0;
+    if (ms <= 0) ms = 2000;
+    return static_cast<unsigned long long>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
+                   uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+                   CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return GEMM_ERR_NO_DEVICE;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * uint64_t(elem_bytes), d0 * d1 * uint64_t(elem_bytes)};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+namespace {
+
+// Shared checks of the BF16 NT family.
+int check_bf16_nt(const void* A, const void* B, const void* C, int M, int N, int K,
+                  size_t c_elem_bytes) {
+  if (!A || !B || !C) return GEMM_ERR_NULL;
+  if (M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_SHAPE;
+  const long long tiles = (long long)((M + 127) / 128) * ((N + 63) / 64);
+  if (tiles > kMaxTiles) return GEMM_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_ALIGN;
+  if (K % 8 != 0) return GEMM_ERR_ALIGN;  // 16-byte row pitch of A and B
+  const size_t sa = size_t(M) * K * 2, sb = size_t(N) * K * 2, sc = size_t(M) * N * c_elem_bytes;
+  if (overlaps(C, sc, A, sa) || overlaps(C, sc, B, sb)) return GEMM_ERR_ALIAS;
+  return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+int gemm_bf16_nt(const void* A, const void* B, void* C, int M, int N, int K, void* stream) {
+  int rc = check_bf16_nt(A, B, C, M, N, K, 2);
+  if (rc != GEMM_OK) return rc;
+  if (N % 8 != 0) return GEMM_ERR_ALIGN;  // 16-byte row pitch of C
+  DeviceInfo dev;
+  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  return launch_gemm_bf16(A, B, C, M, N, K, 0.0f, false, dev, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_inout, int M, int N, int K,
+                            float scale, void* stream) {
+  int rc = check_bf16_nt(A, B, C_inout, M, N, K, 2);
+  if (rc != GEMM_OK) return rc;
+  if (N % 8 != 0) return GEMM_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  return launch_gemm_bf16(A, B, C_inout, M, N, K, scale, true, dev,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int gemm_bf16_nt_ordered(const void* A, const void* B, float* C, int M, int N, int K,
+                         void* stream) {
+  int rc = check_bf16_nt(A, B, C, M, N, K, 4);
+  if (rc != GEMM_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  return launch_gemm_router(A, B, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_nvfp4_bs(const void* a, const void* b, const void* sfa, const void* sfb, void* c, int L,
+                  int M, int N, int K, void* stream) {
+  if (!a || !b || !sfa || !sfb || !c) return GEMM_ERR_NULL;
+  if (L <= 0 || M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_SHAPE;
+  if (M % 128 != 0 || N % 128 != 0 || K % 256 != 0) return GEMM_ERR_SHAPE;
+  const long long tiles = (long long)L * (M / 128) * ((N + 255) / 256);
+  if (tiles > kMaxTiles) return GEMM_ERR_SHAPE;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(c))
+    return GEMM_ERR_ALIGN;
+  const size_t sa = size_t(L) * M * (K / 2), sb = size_t(L) * N * (K / 2);
+  const size_t ssa = size_t(L) * M * (K / 16), ssb = size_t(L) * N * (K / 16);
+  const size_t sc = size_t(L) * M * N * 2;
+  if (overlaps(c, sc, a, sa) || overlaps(c, sc, b, sb) || overlaps(c, sc, sfa, ssa) ||
+      overlaps(c, sc, sfb, ssb))
+    return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != GEMM_OK) return rc;
+  return launch_gemm_nvfp4(a, b, sfa, sfb, c, L, M, N, K, dev, static_cast<cudaStream_t>(stream));
+}
+
+int bf16_scaled_add(void* out, const void* d, float scale, long n, void* stream) {
+  if (!out || !d) return GEMM_ERR_NULL;
+  if (n <= 0) return GEMM_ERR_SHAPE;
+  if (!aligned16(out) || !aligned16(d)) return GEMM_ERR_ALIGN;
+  if (overlaps(out, size_t(n) * 2, d, size_t(n) * 2)) return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != GEMM_OK) return rc;
+  return launch_scaled_add(out, d, scale, n, dev, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_get_device_status(void* stream) {
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != GEMM_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, dev.status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_LAUNCH;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpy(dev.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    return GEMM_ERR_TIMEOUT;
+  }
+  return GEMM_OK;
+}
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_NULL: return "GEMM_ERR_NULL: a required pointer is NULL";
+    case GEMM_ERR_SHAPE: return "GEMM_ERR_SHAPE: invalid dimensions";
+    case GEMM_ERR_ALIGN: return "GEMM_ERR_ALIGN: pointer or row pitch not 16-byte aligned";
+    case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS: output overlaps an input";
+    case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: device is not sm_103";
+    case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: a CUDA call failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel ran out of a bounded wait";
+    case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no usable CUDA device";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Declarations shared by the host-side translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gb300gemm.h"
+
+namespace gb300 {
+
+// Per-device facts the launchers need; filled once per device.
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int cc_major, cc_minor;
+  unsigned int* status;  // device address of the status word
+};
+
+// Fills `out` for the current device.  Returns GEMM_OK, GEMM_ERR_NO_DEVICE
+// or GEMM_ERR_ARCH (not an sm_103 GPU).
+int current_device(DeviceInfo* out);
+
+// Bound on every device-side wait, in nanoseconds (default 2 s; the
+// environment variable GB300GEMM_WAIT_TIMEOUT_MS overrides it).
+unsigned long long wait_timeout_ns();
+
+// Encodes a rank-3 tiled TMA descriptor for a dense row-major tensor
+// [d2][d1][d0] of `elem_bytes`-byte elements starting at `base`, with box
+// {b0, b1, 1}, the given swizzle, zero fill for out-of-bounds elements.
+// Returns GEMM_OK or GEMM_ERR_LAUNCH.
+int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
+                   uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+                   CUtensorMapSwizzle swizzle);
+
+// Launchers; arguments are validated by the caller.
+int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
+                     bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream);
+int launch_gemm_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
+                      int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_gemm_router(const void* A, const void* B, float* C, int M, int N, int K,
+                       const DeviceInfo& dev, cudaStream_t stream);
+int launch_scaled_add(void* out, const void* d, float scale, long n, const DeviceInfo& dev,
+                      cudaStream_t stream);
+
+}  // namespace gb300

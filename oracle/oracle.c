@@ -83,7 +83,7 @@ ORACLE_API uint16_t oracle_f64_to_f16(double x) {
     if (a == 0.0) return sign;
 
     int e2;
-    double fr = frexp(a, &e2);            /* a = fr * 2^e2, fr in [0.5, 1) */
+    (void)frexp(a, &e2);                  /* a = fr * 2^e2, fr in [0.5, 1) */
     /* binary16 normal range: a >= 2^-14, i.e. e2 >= -13.  The quantum
      * (value of one unit in the last place) is 2^(e2-11) for normals and
      * 2^-24 for subnormals. */

@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/gb300gemm.h declares, and rejects bad
+arguments before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gb300gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_scaled_tcgen05_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GB300GEMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"gemm_bf16_nt", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
+            "bf16_scaled_add", "gemm_get_device_status", "gemm_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from nvfp4_block_scaled_tcgen05_gb300 import binding
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "gb300gemm.h"\nint main(void){return gemm_status_string(0)[0]==0;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I",
+                    os.path.join(ROOT, "include"), str(src)], check=True)
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.gemm_status_string(code).decode()
+        assert s.startswith("GEMM_")
+    assert lib.gemm_status_string(99).decode() == "unknown status"
+
+
+P = 0x10000  # a 16-byte aligned fake address; validation never dereferences it
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, P, 2 * P, 8, 8, 8), 1),                 # NULL A
+    ((P, 0, 2 * P, 8, 8, 8), 1),                 # NULL B
+    ((P, 2 * P, 0, 8, 8, 8), 1),                 # NULL C
+    ((P, 2 * P, 3 * P, 0, 8, 8), 2),             # M = 0
+    ((P, 2 * P, 3 * P, 8, -1, 8), 2),            # N < 0
+    ((P, 2 * P, 3 * P, 8, 8, 0), 2),             # K = 0
+    ((P + 8, 2 * P, 3 * P, 8, 8, 8), 3),         # misaligned A
+    ((P, 2 * P, 3 * P, 8, 8, 12), 3),            # K % 8 != 0
+    ((P, 2 * P, 3 * P, 8, 12, 8), 3),            # N % 8 != 0 (C pitch)
+    ((P, 2 * P, P + 64, 8, 8, 8), 4),            # C overlaps A
+])
+def test_gemm_bf16_nt_rejects_bad_arguments(lib, args, expect):
+    assert lib.gemm_bf16_nt(*args, None) == expect
+    assert lib.gemm_bf16_nt_scaled_acc(*args, ctypes.c_float(1.0), None) == expect
+
+
+def test_router_rejects_bad_arguments(lib):
+    assert lib.gemm_bf16_nt_ordered(0, P, 2 * P, 8, 8, 8, None) == 1
+    assert lib.gemm_bf16_nt_ordered(P, 2 * P, 3 * P, 8, 8, 0, None) == 2
+    assert lib.gemm_bf16_nt_ordered(P, 2 * P, 3 * P, 8, 8, 4, None) == 3
+    assert lib.gemm_bf16_nt_ordered(P, 2 * P, 2 * P + 16, 8, 8, 8, None) == 4
+
+
+@pytest.mark.parametrize("dims,expect", [
+    ((1, 128, 128, 256), None),
+    ((0, 128, 128, 256), 2),
+    ((1, 100, 128, 256), 2),      # M % 128
+    ((1, 128, 200, 256), 2),      # N % 128
+    ((1, 128, 128, 128), 2),      # K % 256
+])
+def test_nvfp4_shape_rules(lib, dims, expect):
+    rc = lib.gemm_nvfp4_bs(P, 2 * P, 3 * P, 4 * P, 5 * P, *dims, None)
+    if expect is None:
+        assert rc in (0, 8, 5, 6)  # valid arguments reach the device query
+    else:
+        assert rc == expect
+
+
+def test_nvfp4_pointer_rules(lib):
+    assert lib.gemm_nvfp4_bs(P, 2 * P, 0, 4 * P, 5 * P, 1, 128, 128, 256, None) == 1
+    assert lib.gemm_nvfp4_bs(P, 2 * P, 3 * P + 4, 4 * P, 5 * P, 1, 128, 128, 256, None) == 3
+    # c overlapping sfb
+    assert lib.gemm_nvfp4_bs(P, 2 * P, 3 * P, 4 * P, 4 * P + 1024, 1, 128, 128, 256, None) == 4
+
+
+def test_scaled_add_rules(lib):
+    f = ctypes.c_float(1.0)
+    assert lib.bf16_scaled_add(0, P, f, 10, None) == 1
+    assert lib.bf16_scaled_add(P, 2 * P, f, 0, None) == 2
+    assert lib.bf16_scaled_add(P + 2, 2 * P, f, 10, None) == 3
+    assert lib.bf16_scaled_add(P, P + 16, f, 10, None) == 4
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="a GPU is present")
+def test_valid_call_without_a_gpu_reports_no_device(lib):
+    assert lib.gemm_bf16_nt(P, 2 * P, 3 * P, 8, 8, 8, None) == 8

@@ -1,0 +1,107 @@
+"""GPU parity of the NVFP4 block-scaled GEMM against the oracle: layout
+probes with exact expected values (identity operands, one-hot scales),
+random small cases spanning several tiles, and the full-size problem on
+sampled rows."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_block_scaled_tcgen05_gb300 import synth
+from parity import bits16, check_bitexact16, check_close16, sample_rows, to_dev_u8
+
+pytestmark = pytest.mark.gpu
+UNIT = 0x38     # e4m3 1.0
+ONE = 0x2       # e2m1 1.0
+MAXDQ = 6.0 * 4.0  # largest |e2m1 * scale| of the synthetic inputs
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_block_scaled_tcgen05_gb300 as lib
+    yield lib
+    assert lib.gemm_get_device_status() == 0
+
+
+def run(g, a, b, sfa, sfb, L, M, N, K):
+    c = g.gemm_nvfp4_bs(to_dev_u8(a), to_dev_u8(b), to_dev_u8(sfa), to_dev_u8(sfb), L, M, N, K)
+    return bits16(c).reshape(L * M, N)
+
+
+def identity_codes(L, rows, K):
+    x = np.zeros((L, rows, K // 2), dtype=np.uint8)
+    for r in range(min(rows, K)):
+        x[:, r, r // 2] |= np.uint8(ONE << (4 * (r % 2)))
+    return x
+
+
+def test_identity_b_gives_dequantised_a(g):
+    L, M, N, K = 1, 256, 256, 256
+    a, _, sfa, _ = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 91))
+    b = identity_codes(L, N, K)
+    sfb = np.full(L * N * K // 16, UNIT, dtype=np.uint8)
+    got = run(g, a, b, sfa, sfb, L, M, N, K)
+    check_bitexact16(got, oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K), "identity b",
+                     zero_sign=False)
+
+
+def test_identity_a_gives_dequantised_b_transposed(g):
+    L, M, N, K = 1, 256, 384, 256
+    _, b, _, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 92))
+    a = identity_codes(L, M, K)
+    sfa = np.full(L * M * K // 16, UNIT, dtype=np.uint8)
+    got = run(g, a, b, sfa, sfb, L, M, N, K)
+    check_bitexact16(got, oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K), "identity a")
+
+
+@pytest.mark.parametrize("side", ["a", "b"])
+def test_one_hot_scale(g, side):
+    L, M, N, K = 1, 128, 256, 512
+    a, b, _, _ = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 93))
+    sfa = np.full(L * M * K // 16, UNIT, dtype=np.uint8)
+    sfb = np.full(L * N * K // 16, UNIT, dtype=np.uint8)
+    rest_k = K // 64
+    base = run(g, a, b, sfa, sfb, L, M, N, K)
+    check_close16(base, oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K), K, 6.0, 6.0, "f16",
+                  "unit scales")
+    for (r, j) in [(0, 0), (37, 5), (127, 31), (100, 17)] + ([(200, 9)] if side == "b" else []):
+        s2a, s2b = sfa.copy(), sfb.copy()
+        if side == "a":
+            s2a[oracle.sf_offset(r, j, 0, M // 128, rest_k)] = 0x40
+        else:
+            s2b[oracle.sf_offset(r, j, 0, N // 128, rest_k)] = 0x40
+        got = run(g, a, b, s2a, s2b, L, M, N, K)
+        ref = oracle.gemm_nvfp4_bs(a, b, s2a, s2b, L, M, N, K)
+        check_close16(got, ref, K, 12.0, 6.0, "f16", f"one-hot scale {side} r={r} j={j}")
+        changed = np.argwhere(got != base)
+        if side == "a":
+            assert set(changed[:, 0].tolist()) <= {r}
+        else:
+            assert set(changed[:, 1].tolist()) <= {r}
+
+
+@pytest.mark.parametrize("L,M,N,K", [(1, 128, 256, 256), (1, 384, 640, 1024), (2, 256, 384, 512),
+                                     (1, 128, 128, 256)])
+def test_random_small(g, L, M, N, K):
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 94 + M + N))
+    got = run(g, a, b, sfa, sfb, L, M, N, K)
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K)
+    stats = check_close16(got, ref, K, MAXDQ, MAXDQ, "f16", f"nvfp4 {L}x{M}x{N}x{K}")
+    assert stats["max_ulp"] <= 1, stats
+
+
+def test_full_size_sampled(g):
+    w = synth.NVFP4
+    a, b, sfa, sfb = synth.nvfp4_inputs(w)
+    got = run(g, a, b, sfa, sfb, w.L, w.M, w.N, w.K)
+    rows = np.array(sorted({0, 1, 31, 32, 127, 128, 2047, 2048, 4064, 4095} |
+                           set(np.random.default_rng(9).integers(0, w.M, 22).tolist())))
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, w.L, w.M, w.N, w.K, rows=rows)
+    stats = check_close16(got[rows], ref, w.K, MAXDQ, MAXDQ, "f16", "nvfp4 full size")
+    assert stats["frac_exact"] > 0.9, stats
