@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-warm-s", type=float, default=0.6,
                     help="extra warm-up seconds so that clock samples cover the load")
-    ap.add_argument("--shapes", default="down,qkv,gqa,lora,router,nvfp4",
+    ap.add_argument("--shapes", default="down,qkv,gqa,gqa_splitk,lora,router,nvfp4",
                     help="comma list of the extra shapes to measure")
     ap.add_argument("--no-headline", action="store_true",
                     help="profiling aid: measure only --shapes and print them")
@@ -153,6 +153,16 @@ def time_launches(torch, stream, fn, n_sets, warmup, steps, min_warm_s=0.0):
         end.synchronize()
         t1 = time.time()
     return start.elapsed_time(end) / 1e3 / steps, (t0, t1)
+
+
+def reduce_max(torch, dist, value: float, device) -> float:
+    """Max of `value` over the ranks of the default process group (identity
+    when torch.distributed is not initialised)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def n_sets_for(bytes_per_set: int) -> int:
@@ -270,11 +280,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(torch, dist, x, dev)
 
     def up(x, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(x))
@@ -418,6 +424,9 @@ def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
                     "frac_bf16_peak": tf / bf16_peak})
         del As, Bs, Cs
 
+    if "gqa_splitk" in which:
+        out.append(measure_splitk(torch, lib, synth, up, stream, dev, warmup, reps, check,
+                                  bf16_peak, "gqa", 4))
     if "lora" in which:
         out.append(measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check))
     if "router" in which:
@@ -426,6 +435,32 @@ def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
         out.append(measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_peak))
     assert lib.gemm_get_device_status(sp) == 0
     return out
+
+
+def measure_splitk(torch, lib, synth, up, stream, dev, warmup, reps, check, bf16_peak, name,
+                   splits):
+    """Split-K GEMM (both kernels: FP32 partials + ordered reduce) on one shape."""
+    import ctypes
+    sp = stream.cuda_stream
+    w = synth.BF16_WORKLOADS[name]
+    A_h, B_h = synth.gemm_inputs(w)
+    ws_bytes = int(lib.gemm_bf16_nt_splitk_workspace_bytes(w.M, w.N, w.K, splits))
+    set_bytes = (w.M * w.K + w.N * w.K + w.M * w.N) * 2 + ws_bytes
+    n = n_sets_for(set_bytes)
+    A0, B0 = up(A_h, torch.bfloat16), up(B_h, torch.bfloat16)
+    As = [A0] + [A0.clone() for _ in range(n - 1)]
+    Bs = [B0] + [B0.clone() for _ in range(n - 1)]
+    Cs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    Ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(n)]
+    fn = lambda i: check(lib.gemm_bf16_nt_splitk(As[i].data_ptr(), Bs[i].data_ptr(),
+                                                 Cs[i].data_ptr(), Ws[i].data_ptr(),
+                                                 ctypes.c_size_t(ws_bytes), w.M, w.N, w.K,
+                                                 splits, sp))
+    sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+    del As, Bs, Cs, Ws
+    return {"shape": f"{name}_splitk{splits}", "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6,
+            "TFLOP/s": tf, "frac_bf16_peak": tf / bf16_peak}
 
 
 def measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check):

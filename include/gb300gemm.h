@@ -22,6 +22,8 @@
 #ifndef GB300GEMM_H
 #define GB300GEMM_H
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define GB300GEMM_API __attribute__((visibility("default")))
 #else
@@ -79,6 +81,34 @@ GB300GEMM_API int gemm_bf16_nt(const void* A, const void* B, void* C, int M, int
  */
 GB300GEMM_API int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_inout, int M, int N, int K,
                             float scale, void* stream);
+
+/*
+ * gemm_bf16_nt_splitk - BF16 NT GEMM with the K dimension split into
+ * `k_splits` chunks, for shapes with too few output tiles to fill the GPU:
+ *     partial_s[m,n] = sum over the K blocks of split s of A[m,k] B[n,k]
+ *     C[m,n]         = bf16( ((partial_0 + partial_1) + ...) + partial_{S-1} )
+ * Each split's FP32 partial tile goes to `workspace`; a second kernel adds
+ * the splits in split order (deterministic) and rounds once to BF16.  K is
+ * split in 64-element blocks: S = min(k_splits, ceil(K/64)) reduced so that
+ * no split is empty (gemm_bf16_nt_splitk_workspace_bytes gives the size).
+ *
+ * Defined by: "gemm_dense.rs", dense_gemm_splitk doc comment (partial
+ * products over K_splits chunks into an FP32 workspace of
+ * K_splits*M*N*4 bytes, then a reduce kernel writes BF16).
+ *
+ *   A, B, C, M, N, K as for gemm_bf16_nt;  workspace: caller-owned device
+ *   memory of at least gemm_bf16_nt_splitk_workspace_bytes(M,N,K,k_splits)
+ *   bytes, 16-byte aligned, not overlapping A, B or C; its contents on entry
+ *   are ignored and on return are unspecified;  1 <= k_splits <= 64.
+ * Errors: as gemm_bf16_nt; GEMM_ERR_SHAPE also for a bad k_splits or a
+ * workspace that is too small.
+ */
+GB300GEMM_API int gemm_bf16_nt_splitk(const void* A, const void* B, void* C, void* workspace,
+                                      size_t workspace_bytes, int M, int N, int K, int k_splits,
+                                      void* stream);
+
+/* Workspace bytes gemm_bf16_nt_splitk needs for these arguments (0 if invalid). */
+GB300GEMM_API size_t gemm_bf16_nt_splitk_workspace_bytes(int M, int N, int K, int k_splits);
 
 /*
  * gemm_bf16_nt_ordered - order-preserving "router" GEMM with FP32 output:
@@ -151,6 +181,18 @@ GB300GEMM_API int bf16_scaled_add(void* out, const void* d, float scale, long n,
  * Library extension (the pages define no such call).
  */
 GB300GEMM_API int gemm_get_device_status(void* stream);
+
+/*
+ * gemm_selftest_wait_timeout - diagnostic of the failure path.  Launches one
+ * CTA that waits, through the same bounded wait the GEMM kernels use, on a
+ * barrier that nothing ever arrives on, with the limit `timeout_ms`
+ * (1..10000).  The wait gives up, records a timeout in the device status
+ * word and the kernel returns normally; the next gemm_get_device_status()
+ * returns GEMM_ERR_TIMEOUT and the CUDA context stays usable.
+ * Library extension (the pages define no such call).
+ * Errors: GEMM_ERR_SHAPE (timeout out of range), _ARCH, _NO_DEVICE, _LAUNCH.
+ */
+GB300GEMM_API int gemm_selftest_wait_timeout(int timeout_ms, void* stream);
 
 /* gemm_status_string - static, human-readable name of a status code. */
 GB300GEMM_API const char* gemm_status_string(int status);

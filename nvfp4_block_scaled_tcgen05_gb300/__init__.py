@@ -8,8 +8,11 @@ from .binding import (  # noqa: F401
     gemm_bf16_nt,
     gemm_bf16_nt_ordered,
     gemm_bf16_nt_scaled_acc,
+    gemm_bf16_nt_splitk,
+    gemm_bf16_nt_splitk_workspace_bytes,
     gemm_get_device_status,
     gemm_nvfp4_bs,
+    gemm_selftest_wait_timeout,
     library_path,
     load,
     status_string,

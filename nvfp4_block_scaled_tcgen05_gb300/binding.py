@@ -25,7 +25,9 @@ STATUS = {
     8: "GEMM_ERR_NO_DEVICE",
 }
 EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
-           "bf16_scaled_add", "gemm_get_device_status", "gemm_status_string")
+           "gemm_bf16_nt_splitk",
+           "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
+           "gemm_status_string")
 
 
 class GemmError(RuntimeError):
@@ -55,7 +57,11 @@ def load() -> ctypes.CDLL:
             lib.gemm_bf16_nt_ordered.argtypes = [vp, vp, vp, i, i, i, vp]
             lib.gemm_nvfp4_bs.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
             lib.bf16_scaled_add.argtypes = [vp, vp, f, l, vp]
+            lib.gemm_bf16_nt_splitk.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
+            lib.gemm_bf16_nt_splitk_workspace_bytes.argtypes = [i, i, i, i]
+            lib.gemm_bf16_nt_splitk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_get_device_status.argtypes = [vp]
+            lib.gemm_selftest_wait_timeout.argtypes = [i, vp]
             lib.gemm_status_string.argtypes = [i]
             lib.gemm_status_string.restype = ctypes.c_char_p
             for name in EXPORTS[:-1]:
@@ -129,6 +135,35 @@ def gemm_bf16_nt_scaled_acc(A: torch.Tensor, B: torch.Tensor, C_inout: torch.Ten
     return C_inout
 
 
+def gemm_bf16_nt_splitk_workspace_bytes(M: int, N: int, K: int, k_splits: int) -> int:
+    return int(load().gemm_bf16_nt_splitk_workspace_bytes(M, N, K, k_splits))
+
+
+def gemm_bf16_nt_splitk(A: torch.Tensor, B: torch.Tensor, k_splits: int,
+                        workspace: torch.Tensor | None = None, C: torch.Tensor | None = None,
+                        stream=None):
+    """C = bf16(sum over K splits of FP32 partials), split-K with a caller workspace."""
+    _mat(A, torch.bfloat16, "A")
+    _mat(B, torch.bfloat16, "B")
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    need = gemm_bf16_nt_splitk_workspace_bytes(M, N, K, k_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=A.device)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _mat(C, torch.bfloat16, "C")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().gemm_bf16_nt_splitk(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                      workspace.data_ptr(), nbytes, M, N, K, int(k_splits),
+                                      _stream_ptr(stream)), "gemm_bf16_nt_splitk")
+    return C
+
+
 def gemm_bf16_nt_ordered(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
                          stream=None):
     """FP32 C = strict-order, FMA-free A . B^T on CUDA cores (router GEMM)."""
@@ -175,6 +210,12 @@ def bf16_scaled_add(out: torch.Tensor, d: torch.Tensor, scale: float, stream=Non
     _check(load().bf16_scaled_add(out.data_ptr(), d.data_ptr(), float(scale), out.numel(),
                                   _stream_ptr(stream)), "bf16_scaled_add")
     return out
+
+
+def gemm_selftest_wait_timeout(timeout_ms: int = 50, stream=None) -> None:
+    """Launch the failure-path self test (a wait that must run out)."""
+    _check(load().gemm_selftest_wait_timeout(int(timeout_ms), _stream_ptr(stream)),
+           "gemm_selftest_wait_timeout")
 
 
 def gemm_get_device_status(stream=None) -> int:

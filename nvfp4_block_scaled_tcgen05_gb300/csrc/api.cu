@@ -161,6 +161,35 @@ int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_inout, int M, 
                           static_cast<cudaStream_t>(stream));
 }
 
+int gemm_bf16_nt_splitk(const void* A, const void* B, void* C, void* workspace,
+                        size_t workspace_bytes, int M, int N, int K, int k_splits, void* stream) {
+  int rc = check_bf16_nt(A, B, C, M, N, K, 2);
+  if (rc != GEMM_OK) return rc;
+  if (N % 8 != 0) return GEMM_ERR_ALIGN;
+  if (!workspace) return GEMM_ERR_NULL;
+  if (k_splits < 1 || k_splits > 64) return GEMM_ERR_SHAPE;
+  if (!aligned16(workspace)) return GEMM_ERR_ALIGN;
+  int kbps = 0;
+  const int s_eff = splitk_effective_splits(K, k_splits, &kbps);
+  const size_t need = size_t(s_eff) * size_t(M) * size_t(N) * 4;
+  if (workspace_bytes < need) return GEMM_ERR_SHAPE;
+  const size_t sa = size_t(M) * K * 2, sb = size_t(N) * K * 2, sc = size_t(M) * N * 2;
+  if (overlaps(workspace, need, A, sa) || overlaps(workspace, need, B, sb) ||
+      overlaps(workspace, need, C, sc))
+    return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  return launch_gemm_bf16_splitk(A, B, C, static_cast<float*>(workspace), M, N, K, k_splits, dev,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+size_t gemm_bf16_nt_splitk_workspace_bytes(int M, int N, int K, int k_splits) {
+  if (M <= 0 || N <= 0 || K <= 0 || k_splits < 1 || k_splits > 64) return 0;
+  int kbps = 0;
+  const int s_eff = splitk_effective_splits(K, k_splits, &kbps);
+  return size_t(s_eff) * size_t(M) * size_t(N) * 4;
+}
+
 int gemm_bf16_nt_ordered(const void* A, const void* B, float* C, int M, int N, int K,
                          void* stream) {
   int rc = check_bf16_nt(A, B, C, M, N, K, 4);
@@ -219,6 +248,14 @@ int gemm_get_device_status(void* stream) {
     return GEMM_ERR_TIMEOUT;
   }
   return GEMM_OK;
+}
+
+int gemm_selftest_wait_timeout(int timeout_ms, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return GEMM_ERR_SHAPE;
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != GEMM_OK) return rc;
+  return launch_selftest_timeout(timeout_ms, dev, static_cast<cudaStream_t>(stream));
 }
 
 const char* gemm_status_string(int status) {

@@ -36,7 +36,50 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// C[i] = bf16(ws[0][i] + ws[1][i] + ... + ws[S-1][i]), FP32 adds in split
+// order (deterministic); 8 outputs per thread, 16-byte accesses.
+__global__ void __launch_bounds__(kThreads)
+    splitk_reduce_kernel(const float* __restrict__ ws, uint16_t* __restrict__ C, size_t n,
+                         int splits) {
+  const size_t nvec = n / 8;
+  const size_t stride = size_t(gridDim.x) * kThreads;
+  for (size_t i = size_t(blockIdx.x) * kThreads + threadIdx.x; i < nvec; i += stride) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(ws) + 2 * i);
+    float4 b = __ldg(reinterpret_cast<const float4*>(ws) + 2 * i + 1);
+    for (int s = 1; s < splits; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(ws + size_t(s) * n) + 2 * i;
+      const float4 x = __ldg(src), y = __ldg(src + 1);
+      a.x = __fadd_rn(a.x, x.x); a.y = __fadd_rn(a.y, x.y);
+      a.z = __fadd_rn(a.z, x.z); a.w = __fadd_rn(a.w, x.w);
+      b.x = __fadd_rn(b.x, y.x); b.y = __fadd_rn(b.y, y.y);
+      b.z = __fadd_rn(b.z, y.z); b.w = __fadd_rn(b.w, y.w);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(__float_as_uint(a.x), __float_as_uint(a.y));
+    o.y = pack_bf16x2(__float_as_uint(a.z), __float_as_uint(a.w));
+    o.z = pack_bf16x2(__float_as_uint(b.x), __float_as_uint(b.y));
+    o.w = pack_bf16x2(__float_as_uint(b.z), __float_as_uint(b.w));
+    reinterpret_cast<uint4*>(C)[i] = o;
+  }
+  const size_t tail = n - nvec * 8;
+  if (blockIdx.x == 0 && threadIdx.x < tail) {
+    const size_t idx = nvec * 8 + threadIdx.x;
+    float a = ws[idx];
+    for (int s = 1; s < splits; ++s) a = __fadd_rn(a, ws[size_t(s) * n + idx]);
+    C[idx] = uint16_t(pack_bf16x2(__float_as_uint(a), 0u) & 0xFFFFu);
+  }
+}
+
 }  // namespace
+
+int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
+                         cudaStream_t stream) {
+  const size_t nvec = n / 8;
+  const size_t want = (nvec + kThreads - 1) / kThreads;
+  const int grid = int(std::max<size_t>(1, std::min<size_t>(want, size_t(dev.num_sms) * 8)));
+  splitk_reduce_kernel<<<grid, kThreads, 0, stream>>>(ws, static_cast<uint16_t*>(C), n, splits);
+  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
 
 int launch_scaled_add(void* out, const void* d, float scale, long n, const DeviceInfo& dev,
                       cudaStream_t stream) {

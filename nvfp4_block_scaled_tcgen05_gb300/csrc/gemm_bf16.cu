@@ -1,42 +1,37 @@
 // BF16 NT GEMM and the fused scaled-acc (LoRA expand+fold) epilogue on
-// tcgen05 kind::f16.  Tile 128 x 256 x 64, 4-stage TMA ring, two TMEM
-// accumulators so the epilogue of one tile overlaps the next tile's K loop.
-#include <algorithm>
-#include <atomic>
-
-#include "internal.h"
-#include "tcgen05_gemm.cuh"
+// tcgen05 kind::f16, FP32 accumulation in TMEM.
+//
+// Two tile configurations, chosen per shape:
+//  * pair (cta_group::2): 256 x 256 tiles shared by two SMs, each staging its
+//    128 A rows and 128 of the 256 B rows per 64-deep K step (32 KB per stage,
+//    6 stages), two TMEM accumulators per CTA;
+//  * single (cta_group::1): 128 x 256 tiles, 48 KB stages, 4 stages; used when
+//    there are fewer pair tiles than SM pairs.
+// The scaled-acc epilogue of a short-K GEMM (the LoRA fold, K = rank) is
+// bound by reading and writing the output; its configurations trade
+// pipeline stages for eight output buffers per epilogue warp so the old
+// output of the next tile streams in while the current tile is written.
+// The MMA sequence of a tile does not depend on the stage count, so every
+// configuration with the same CTA group produces the same accumulators.
+#include "launch.cuh"
 
 namespace gb300 {
 
-using Bf16Cfg = TileCfg<Operand::kBF16, 256, 4>;
+using Bf16Pair = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;
+using Bf16Single = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2>;
+using Bf16PairStream = TileCfg<Operand::kBF16, 2, 256, 3, 4, 8>;
+using Bf16SingleStream = TileCfg<Operand::kBF16, 1, 256, 2, 4, 8>;
+constexpr int kStreamMaxK = 256;  // scaled-acc K up to this uses the streaming configurations
 
-template <class Cfg, Epilogue EPI>
-static int launch_tcgen05(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                          const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream) {
-  auto kern = tcgen05_gemm_kernel<Cfg, EPI>;
-  static std::atomic<unsigned long long> configured{0};
-  const unsigned long long bit = 1ull << (dev.device & 63);
-  if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
-        cudaSuccess)
-      return GEMM_ERR_LAUNCH;
-    configured.fetch_or(bit);
-  }
-  const int grid = std::min(p.total_tiles, dev.num_sms);
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tc, p);
-  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
-}
-
-int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
-                     bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
-  using Cfg = Bf16Cfg;
+template <class Cfg>
+static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
+                    bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
   CUtensorMap ta, tb, tc;
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
                           64, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(K), uint64_t(N), 1,
-                        64, Cfg::BN, CU_TENSOR_MAP_SWIZZLE_128B);
+                        64, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, uint64_t(N), uint64_t(M), 1,
                         64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -46,15 +41,84 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   p.N = N;
   p.K = K;
   p.L = 1;
-  p.num_m_blocks = (M + Cfg::BM - 1) / Cfg::BM;
+  p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
   p.total_tiles = p.num_m_blocks * p.num_n_blocks;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blocks;
   p.scale = scale;
   p.status = dev.status;
   p.timeout_ns = wait_timeout_ns();
-  return scaled_acc ? launch_tcgen05<Cfg, Epilogue::kScaledAccBF16>(ta, tb, tc, p, dev, stream)
-                    : launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, p, dev, stream);
+  // the scale-factor maps are unused for BF16; pass A's map in their place
+  return scaled_acc
+             ? launch_tcgen05<Cfg, Epilogue::kScaledAccBF16>(ta, tb, tc, ta, ta, p, dev, stream)
+             : launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, ta, ta, p, dev, stream);
+}
+
+// Split-K: split s of the K blocks [s*kbps, (s+1)*kbps) writes its FP32
+// partial tile into workspace[s][M][N]; a second kernel sums the splits in
+// order s = 0..S-1 and rounds to BF16 ("gemm_dense.rs", dense_gemm_splitk).
+template <class Cfg>
+static int run_bf16_splitk(const void* A, const void* B, float* ws, int M, int N, int K,
+                           int splits, int kbps, const DeviceInfo& dev, cudaStream_t stream) {
+  CUtensorMap ta, tb, tw;
+  int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
+                          64, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(K), uint64_t(N), 1,
+                        64, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, uint64_t(N), uint64_t(M),
+                        uint64_t(splits), 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != GEMM_OK) return rc;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.L = splits;
+  p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
+  p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
+  p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
+  p.total_tiles = p.num_m_blocks * p.num_n_blocks * splits;
+  p.k_splits = splits;
+  p.kb_per_split = kbps;
+  p.status = dev.status;
+  p.timeout_ns = wait_timeout_ns();
+  return launch_tcgen05<Cfg, Epilogue::kStoreF32>(ta, tb, tw, ta, ta, p, dev, stream);
+}
+
+int splitk_effective_splits(int K, int splits, int* kb_per_split) {
+  const int nkb = (K + 63) / 64;
+  if (splits > nkb) splits = nkb;
+  const int kbps = (nkb + splits - 1) / splits;
+  *kb_per_split = kbps;
+  return (nkb + kbps - 1) / kbps;  // every split non-empty
+}
+
+int launch_gemm_bf16_splitk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
+                            int splits, const DeviceInfo& dev, cudaStream_t stream) {
+  int kbps = 0;
+  const int s_eff = splitk_effective_splits(K, splits, &kbps);
+  const long long pair_units = (long long)((M + 255) / 256) * ((N + 255) / 256) * s_eff;
+  int cg = (pair_units >= dev.num_sms / 2) ? 2 : 1;
+  if (const int o = cta_group_override()) cg = o;
+  const int rc = cg == 2 ? run_bf16_splitk<Bf16Pair>(A, B, ws, M, N, K, s_eff, kbps, dev, stream)
+                         : run_bf16_splitk<Bf16Single>(A, B, ws, M, N, K, s_eff, kbps, dev, stream);
+  if (rc != GEMM_OK) return rc;
+  return launch_splitk_reduce(ws, C, size_t(M) * N, s_eff, dev, stream);
+}
+
+int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
+                     bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
+  const long long pair_tiles = (long long)((M + 255) / 256) * ((N + 255) / 256);
+  int cg = (pair_tiles >= dev.num_sms / 2) ? 2 : 1;
+  if (const int o = cta_group_override()) cg = o;
+  if (scaled_acc && K <= kStreamMaxK)
+    return cg == 2 ? run_bf16<Bf16PairStream>(A, B, C, M, N, K, scale, true, dev, stream)
+                   : run_bf16<Bf16SingleStream>(A, B, C, M, N, K, scale, true, dev, stream);
+  return cg == 2 ? run_bf16<Bf16Pair>(A, B, C, M, N, K, scale, scaled_acc, dev, stream)
+                 : run_bf16<Bf16Single>(A, B, C, M, N, K, scale, scaled_acc, dev, stream);
 }
 
 }  // namespace gb300

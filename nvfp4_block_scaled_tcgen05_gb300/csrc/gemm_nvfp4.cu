@@ -1,63 +1,74 @@
 // NVFP4 block-scaled GEMM on tcgen05 kind::mxf4nvf4 (scale_vec::4X): packed
 // e2m1 operands, one e4m3 scale per 16 K elements in the hardware scale
 // layout ("kernelbot nvfp4 gemm submission 123329", sections "NVIDIA Block
-// layout" / "Layout semantics"), FP16 output.  Tile 128 x 256 x 256, 3-stage
-// ring; each stage also carries the 4 consecutive 512-byte scale atoms of
-// the A rows and of each 128-row half of the B rows, which tcgen05.cp moves
-// into a per-stage TMEM slot before the 4 MMAs of the stage.
-#include <algorithm>
-#include <atomic>
-
-#include "internal.h"
-#include "tcgen05_gemm.cuh"
+// layout" / "Layout semantics"), FP16 output.
+//
+// Each 256-element K stage carries, per 128 rows, the 4 consecutive 512-byte
+// scale atoms of that K range (2 KB, contiguous in the hardware layout);
+// they are TMA-loaded as one 256 x u64 box and tcgen05.cp'd into a per-stage
+// TMEM slot ahead of the stage's 4 MMAs.  One TMEM accumulator (256 columns)
+// plus the scale slots fill the 512 columns, so the epilogue is
+// register-staged: 8 warps read the whole accumulator, release it, then
+// convert and store while the next tile's MMAs run.
+//
+// Configurations: pair (cta_group::2, 256 x 256 tiles, each CTA stages its
+// 128 A rows, 128 B rows and the scales of all 256 B rows, 5 stages) and
+// single (cta_group::1, 128 x 256 tiles, 3 stages) for small problems.
+#include "launch.cuh"
 
 namespace gb300 {
 
-using Nvfp4Cfg = TileCfg<Operand::kNVFP4, 256, 3>;
+using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 1>;
+using Nvfp4Single = TileCfg<Operand::kNVFP4, 1, 256, 3, 8, 1>;
 
-int launch_gemm_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
-                      int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  using Cfg = Nvfp4Cfg;
-  CUtensorMap ta, tb, tc;
+template <class Cfg>
+static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
+                     int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  CUtensorMap ta, tb, tc, tsa, tsb;
   const uint64_t kb = uint64_t(K) / 2;  // bytes per packed row
+  const int rest_m = M / 128, rest_n = N / 128, rest_k = K / 64;
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, kb, uint64_t(M), uint64_t(L),
                           128, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, kb, uint64_t(N), uint64_t(L), 128,
-                        Cfg::BN, CU_TENSOR_MAP_SWIZZLE_128B);
+                        Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c, uint64_t(N), uint64_t(M),
                         uint64_t(L), 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  // scales: one row of rest_k * 512 bytes (= rest_k * 64 u64) per (l, 128-row block)
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sfa, uint64_t(rest_k) * 64,
+                        uint64_t(L) * rest_m, 1, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sfb, uint64_t(rest_k) * 64,
+                        uint64_t(L) * rest_n, 1, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != GEMM_OK) return rc;
   GemmParams p{};
   p.M = M;
   p.N = N;
   p.K = K;
   p.L = L;
-  p.num_m_blocks = M / Cfg::BM;
+  p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = K / Cfg::BK;
   p.total_tiles = p.num_m_blocks * p.num_n_blocks * L;
-  p.rest_m = M / 128;
-  p.rest_n = N / 128;
-  p.rest_k = K / 64;
-  p.sfa = static_cast<const uint8_t*>(sfa);
-  p.sfb = static_cast<const uint8_t*>(sfb);
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blocks;
+  p.rest_m = rest_m;
+  p.rest_n = rest_n;
+  p.rest_k = rest_k;
   p.status = dev.status;
   p.timeout_ns = wait_timeout_ns();
+  return launch_tcgen05<Cfg, Epilogue::kStoreFP16>(ta, tb, tc, tsa, tsb, p, dev, stream);
+}
 
-  auto kern = tcgen05_gemm_kernel<Cfg, Epilogue::kStoreFP16>;
-  static std::atomic<unsigned long long> configured{0};
-  const unsigned long long bit = 1ull << (dev.device & 63);
-  if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
-        cudaSuccess)
-      return GEMM_ERR_LAUNCH;
-    configured.fetch_or(bit);
-  }
-  const int grid = std::min(p.total_tiles, dev.num_sms);
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tc, p);
-  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+int launch_gemm_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
+                      int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  const long long pair_tiles = (long long)L * ((M + 255) / 256) * ((N + 255) / 256);
+  int cg = (pair_tiles >= dev.num_sms / 2) ? 2 : 1;
+  if (const int o = cta_group_override()) cg = o;
+  return cg == 2 ? run_nvfp4<Nvfp4Pair>(a, b, sfa, sfb, c, L, M, N, K, dev, stream)
+                 : run_nvfp4<Nvfp4Single>(a, b, sfa, sfb, c, L, M, N, K, dev, stream);
 }
 
 }  // namespace gb300

@@ -6,8 +6,10 @@
 //
 // Register blocking: each thread owns a TM x TN block of outputs; BK-deep
 // slices of A and B are widened to FP32 once and staged k-major in shared
-// memory (double-buffered), so the inner loop is two 16-byte loads of A,
-// one of B and TM*TN multiply/add pairs.
+// memory (double-buffered), so the inner loop is one 16-byte load of A, one
+// of B and TM*TN multiply/add pairs.  32 x 64 block tiles (564 blocks for
+// the 4510 x 256 router, ~15 resident warps per SM) keep the FP32 pipes fed
+// and the blocks evenly spread over the SMs.
 #include <algorithm>
 
 #include "internal.h"
@@ -16,7 +18,7 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kBM = 64, kBN = 64, kBK = 32, kTM = 8, kTN = 4;
+constexpr int kBM = 32, kBN = 64, kBK = 32, kTM = 4, kTN = 4;
 constexpr int kTX = kBN / kTN;  // 16 threads along n
 constexpr int kTY = kBM / kTM;  // 8 threads along m
 constexpr int kThreads = kTX * kTY;
@@ -43,16 +45,19 @@ __global__ void __launch_bounds__(kThreads)
   const int tx = tid % kTX, ty = tid / kTX;
   const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
 
-  constexpr int A_PER_T = kBM * kChunks / kThreads;  // 2
+  constexpr int A_PER_T = kBM * kChunks / kThreads;  // 1
   constexpr int B_PER_T = kBN * kChunks / kThreads;  // 2
   static_assert(A_PER_T * kThreads == kBM * kChunks && B_PER_T * kThreads == kBN * kChunks, "");
   uint4 ra[A_PER_T], rb[B_PER_T];
 
+  // Chunk id -> (row, 16-byte chunk): consecutive threads take consecutive
+  // rows of one chunk column, so the transposed shared-memory stores of a
+  // warp hit 32 different banks.
   auto gload = [&](int k0) {
 #pragma unroll
     for (int i = 0; i < A_PER_T; ++i) {
       const int id = tid + i * kThreads;
-      const int row = id / kChunks, ch = id % kChunks;
+      const int row = id % kBM, ch = id / kBM;
       const int gm = m0 + row, gk = k0 + ch * 8;
       ra[i] = (gm < M && gk < K) ? __ldg(reinterpret_cast<const uint4*>(A + size_t(gm) * K + gk))
                                  : make_uint4(0, 0, 0, 0);
@@ -60,7 +65,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < B_PER_T; ++i) {
       const int id = tid + i * kThreads;
-      const int row = id / kChunks, ch = id % kChunks;
+      const int row = id % kBN, ch = id / kBN;
       const int gn = n0 + row, gk = k0 + ch * 8;
       rb[i] = (gn < N && gk < K) ? __ldg(reinterpret_cast<const uint4*>(B + size_t(gn) * K + gk))
                                  : make_uint4(0, 0, 0, 0);
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < A_PER_T; ++i) {
       const int id = tid + i * kThreads;
-      const int row = id / kChunks, ch = id % kChunks;
+      const int row = id % kBM, ch = id / kBM;
       float f[8];
       widen8(ra[i], f);
 #pragma unroll
@@ -79,7 +84,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < B_PER_T; ++i) {
       const int id = tid + i * kThreads;
-      const int row = id / kChunks, ch = id % kChunks;
+      const int row = id % kBN, ch = id / kBN;
       float f[8];
       widen8(rb[i], f);
 #pragma unroll
@@ -93,11 +98,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < kTN; ++j) acc[i][j] = 0.0f;
 
+  static_assert(kTM == 4 && kTN == 4, "one float4 of A and one of B per k");
   auto step = [&](int buf, int kk) {
     const float4 a0 = *reinterpret_cast<const float4*>(&sA[buf][kk][ty * kTM]);
-    const float4 a1 = *reinterpret_cast<const float4*>(&sA[buf][kk][ty * kTM + 4]);
     const float4 b0 = *reinterpret_cast<const float4*>(&sB[buf][kk][tx * kTN]);
-    const float a[kTM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float a[kTM] = {a0.x, a0.y, a0.z, a0.w};
     const float b[kTN] = {b0.x, b0.y, b0.z, b0.w};
 #pragma unroll
     for (int i = 0; i < kTM; ++i)

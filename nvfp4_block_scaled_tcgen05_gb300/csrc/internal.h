@@ -43,5 +43,15 @@ int launch_gemm_router(const void* A, const void* B, float* C, int M, int N, int
                        const DeviceInfo& dev, cudaStream_t stream);
 int launch_scaled_add(void* out, const void* d, float scale, long n, const DeviceInfo& dev,
                       cudaStream_t stream);
+int launch_selftest_timeout(int timeout_ms, const DeviceInfo& dev, cudaStream_t stream);
+
+// Split-K: clamps `splits` to the number of 64-deep K blocks and returns the
+// number of non-empty splits actually used (and the K blocks per split).
+int splitk_effective_splits(int K, int splits, int* kb_per_split);
+int launch_gemm_bf16_splitk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
+                            int splits, const DeviceInfo& dev, cudaStream_t stream);
+// C[i] = bf16(sum_{s=0..S-1} ws[s*n + i]) in split order.
+int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
+                         cudaStream_t stream);
 
 }  // namespace gb300

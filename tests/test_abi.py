@@ -116,3 +116,23 @@ def test_scaled_add_rules(lib):
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="a GPU is present")
 def test_valid_call_without_a_gpu_reports_no_device(lib):
     assert lib.gemm_bf16_nt(P, 2 * P, 3 * P, 8, 8, 8, None) == 8
+
+
+def test_splitk_workspace_size_rules(lib):
+    ws = lib.gemm_bf16_nt_splitk_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(5120, 512, 2048, 4) == 4 * 5120 * 512 * 4
+    assert ws(300, 520, 200, 3) == 2 * 300 * 520 * 4   # 4 K blocks: 2 per split, 2 splits
+    assert ws(64, 64, 64, 8) == 1 * 64 * 64 * 4        # one K block: one split
+    assert ws(0, 8, 8, 1) == 0 and ws(8, 8, 8, 0) == 0 and ws(8, 8, 8, 65) == 0
+
+
+def test_splitk_rejects_bad_arguments(lib):
+    f = lib.gemm_bf16_nt_splitk
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_size_t] + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    big = 1 << 30
+    assert f(P, 2 * P, 3 * P, 0, big, 8, 8, 64, 2, None) == 1          # NULL workspace
+    assert f(P, 2 * P, 3 * P, 4 * P, big, 8, 8, 64, 0, None) == 2      # k_splits < 1
+    assert f(P, 2 * P, 3 * P, 4 * P, 16, 64, 64, 256, 2, None) == 2    # workspace too small
+    assert f(P, 2 * P, 3 * P, 4 * P + 8, big, 8, 8, 64, 2, None) == 3  # misaligned workspace
+    assert f(P, 2 * P, 3 * P, P + 16, big, 8, 8, 64, 2, None) == 4     # workspace overlaps A

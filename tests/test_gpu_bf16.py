@@ -25,6 +25,13 @@ def g():
     assert lib.gemm_get_device_status() == 0
 
 
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
+def cg(request, monkeypatch):
+    """Force the single-CTA or the CTA-pair (cta_group::2) kernel."""
+    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(request.param))
+    return request.param
+
+
 def amax(x):
     return float(np.abs(bf16_val(x)).max())
 
@@ -42,7 +49,7 @@ def run_gemm(g, A, B):
     (17, 1000, 1032),    # many K blocks with a tail
     (640, 768, 64),      # exact multiples
 ])
-def test_gemm_bf16_ragged(g, M, N, K):
+def test_gemm_bf16_ragged(g, cg, M, N, K):
     A = synth.bf16_normal((M, K), 1.0, 11 + M)
     B = synth.bf16_normal((N, K), 1.0, 12 + N)
     got = run_gemm(g, A, B)
@@ -50,14 +57,14 @@ def test_gemm_bf16_ragged(g, M, N, K):
     check_close16(got, ref, K, amax(A), amax(B), what=f"gemm {M}x{N}x{K}")
 
 
-def test_gemm_bf16_exact_integers_bitexact(g):
+def test_gemm_bf16_exact_integers_bitexact(g, cg):
     M, N, K = 384, 520, 512
     A = synth.bf16_small_ints((M, K), -3, 3, 21)
     B = synth.bf16_small_ints((N, K), -3, 3, 22)
     check_bitexact16(run_gemm(g, A, B), oracle.gemm_bf16_nt(A, B), "exact integers")
 
 
-def test_gemm_bf16_identity_and_permutation(g):
+def test_gemm_bf16_identity_and_permutation(g, cg):
     M, K = 300, 256
     A = synth.bf16_normal((M, K), 1.0, 23)
     eye = np.zeros((K, K), dtype=np.uint16)
@@ -69,7 +76,7 @@ def test_gemm_bf16_identity_and_permutation(g):
     check_bitexact16(run_gemm(g, A, P), A[:, perm], "permutation")
 
 
-def test_gemm_bf16_many_tiles_per_cta(g):
+def test_gemm_bf16_many_tiles_per_cta(g, cg):
     # 32 x 16 = 512 tiles: every CTA walks several tiles and both TMEM buffers
     M, N, K = 4096, 4096, 128
     A = synth.bf16_normal((M, K), 1.0, 31)
@@ -80,7 +87,7 @@ def test_gemm_bf16_many_tiles_per_cta(g):
     check_close16(got[rows], ref, K, amax(A), amax(B), what="many tiles")
 
 
-def test_gemm_bf16_no_write_outside_c(g):
+def test_gemm_bf16_no_write_outside_c(g, cg):
     M, N, K = 200, 264, 64
     A = synth.bf16_normal((M, K), 1.0, 41)
     B = synth.bf16_normal((N, K), 1.0, 42)
@@ -119,7 +126,7 @@ def test_scaled_acc_tiny_config(g):
 
 @pytest.mark.parametrize("M,N,K,scale", [(128, 256, 256, 0.5), (300, 520, 200, 2.0),
                                          (257, 1032, 16, -0.375), (64, 64, 24, 1.0)])
-def test_scaled_acc_fused_equals_unfused_bitexact(g, M, N, K, scale):
+def test_scaled_acc_fused_equals_unfused_bitexact(g, cg, M, N, K, scale):
     A = synth.bf16_normal((M, K), 1.0, 51 + K)
     B = synth.bf16_normal((N, K), 0.5, 52 + K)
     out0 = synth.bf16_normal((M, N), 1.0, 53 + K)

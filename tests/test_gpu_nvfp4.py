@@ -29,6 +29,13 @@ def g():
     assert lib.gemm_get_device_status() == 0
 
 
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
+def cg(request, monkeypatch):
+    """Force the single-CTA or the CTA-pair (cta_group::2) kernel."""
+    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(request.param))
+    return request.param
+
+
 def run(g, a, b, sfa, sfb, L, M, N, K):
     c = g.gemm_nvfp4_bs(to_dev_u8(a), to_dev_u8(b), to_dev_u8(sfa), to_dev_u8(sfb), L, M, N, K)
     return bits16(c).reshape(L * M, N)
@@ -41,7 +48,7 @@ def identity_codes(L, rows, K):
     return x
 
 
-def test_identity_b_gives_dequantised_a(g):
+def test_identity_b_gives_dequantised_a(g, cg):
     L, M, N, K = 1, 256, 256, 256
     a, _, sfa, _ = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 91))
     b = identity_codes(L, N, K)
@@ -51,7 +58,7 @@ def test_identity_b_gives_dequantised_a(g):
                      zero_sign=False)
 
 
-def test_identity_a_gives_dequantised_b_transposed(g):
+def test_identity_a_gives_dequantised_b_transposed(g, cg):
     L, M, N, K = 1, 256, 384, 256
     _, b, _, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 92))
     a = identity_codes(L, M, K)
@@ -61,7 +68,7 @@ def test_identity_a_gives_dequantised_b_transposed(g):
 
 
 @pytest.mark.parametrize("side", ["a", "b"])
-def test_one_hot_scale(g, side):
+def test_one_hot_scale(g, cg, side):
     L, M, N, K = 1, 128, 256, 512
     a, b, _, _ = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 93))
     sfa = np.full(L * M * K // 16, UNIT, dtype=np.uint8)
@@ -87,8 +94,8 @@ def test_one_hot_scale(g, side):
 
 
 @pytest.mark.parametrize("L,M,N,K", [(1, 128, 256, 256), (1, 384, 640, 1024), (2, 256, 384, 512),
-                                     (1, 128, 128, 256)])
-def test_random_small(g, L, M, N, K):
+                                     (1, 128, 128, 256), (2, 384, 512, 256), (1, 512, 768, 2048)])
+def test_random_small(g, cg, L, M, N, K):
     a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 94 + M + N))
     got = run(g, a, b, sfa, sfb, L, M, N, K)
     ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K)
