@@ -111,6 +111,39 @@ GB300GEMM_API int gemm_bf16_nt_splitk(const void* A, const void* B, void* C, voi
 GB300GEMM_API size_t gemm_bf16_nt_splitk_workspace_bytes(int M, int N, int K, int k_splits);
 
 /*
+ * gemm_bf16_nt_splitk_static - gemm_bf16_nt_splitk without a workspace
+ * argument, for callers that cannot allocate device memory: code whose host
+ * framework owns the whole device pool and forbids other allocations,
+ * serving loops that must not call the CUDA allocator after warm-up (an
+ * allocation can synchronise the device), and plugins handed raw pointers
+ * but no allocator.  The pages have no counterpart; it is a library
+ * extension.
+ *
+ * The FP32 partial tiles go to a fixed scratch array of
+ * GEMM_SPLITK_STATIC_SCRATCH_BYTES that is part of the library's device
+ * image: every GPU that loads the library holds it until the process exits.
+ * This call allocates nothing and frees nothing.  The caller still passes
+ * A, B and C exactly as for gemm_bf16_nt_splitk, and the result is the same.
+ *
+ *   Limit: S * M * N * 4 <= GEMM_SPLITK_STATIC_SCRATCH_BYTES, with S the
+ *   splits actually used (gemm_bf16_nt_splitk_workspace_bytes); larger
+ *   problems are rejected with GEMM_ERR_SHAPE before anything is launched.
+ *   The first call on each device looks up the scratch array's device
+ *   address (cudaGetSymbolAddress with that device current); make that first
+ *   call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents; no
+ *   element needs to start at zero (each call writes every element it reads
+ *   before reading it).  Calls whose executions overlap on the GPU (other
+ *   streams, other host threads) race on the array and give wrong results:
+ *   order them on one stream or with events.
+ * Errors: GEMM_ERR_NULL, _SHAPE (dims, k_splits, or over the limit),
+ * _ALIGN, _ALIAS, _ARCH, _NO_DEVICE, _LAUNCH.
+ */
+#define GEMM_SPLITK_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+GB300GEMM_API int gemm_bf16_nt_splitk_static(const void* A, const void* B, void* C, int M, int N,
+                                             int K, int k_splits, void* stream);
+
+/*
  * gemm_bf16_nt_ordered - order-preserving "router" GEMM with FP32 output:
  *     C[m,n] = (((0 + A[m,0]B[n,0]) + A[m,1]B[n,1]) + ... + A[m,K-1]B[n,K-1])
  * every product and every sum rounded to FP32 (round to nearest even), no
