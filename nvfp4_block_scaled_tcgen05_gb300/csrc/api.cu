@@ -118,6 +118,22 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, 
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
+int encode_tmap_3d_strided(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                           uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                           uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                           CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return GEMM_ERR_NO_DEVICE;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
 namespace {
 
 // Shared checks of the BF16 NT family.

@@ -19,6 +19,7 @@ namespace gb300 {
 
 using Bf16Pair = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;
 using Bf16Single = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2>;
+using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;    // plain BF16 output
 using Bf16PairStream = TileCfg<Operand::kBF16, 2, 256, 3, 4, 8>;
 using Bf16SingleStream = TileCfg<Operand::kBF16, 1, 256, 2, 4, 8>;
 constexpr int kStreamMaxK = 256;  // scaled-acc K up to this uses the streaming configurations
@@ -48,12 +49,17 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blocks;
   p.scale = scale;
+  p.c_ptr = C;
   p.status = dev.status;
   p.timeout_ns = wait_timeout_ns();
   // the scale-factor maps are unused for BF16; pass A's map in their place
-  return scaled_acc
-             ? launch_tcgen05<Cfg, Epilogue::kScaledAccBF16>(ta, tb, tc, ta, ta, p, dev, stream)
-             : launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, ta, ta, p, dev, stream);
+  if constexpr (Cfg::EPI_BUFS == 0) {
+    return launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, ta, ta, p, dev, stream);
+  } else {
+    return scaled_acc
+               ? launch_tcgen05<Cfg, Epilogue::kScaledAccBF16>(ta, tb, tc, ta, ta, p, dev, stream)
+               : launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, ta, ta, p, dev, stream);
+  }
 }
 
 // Split-K: split s of the K blocks [s*kbps, (s+1)*kbps) writes its FP32
@@ -117,6 +123,8 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   if (scaled_acc && K <= kStreamMaxK)
     return cg == 2 ? run_bf16<Bf16PairStream>(A, B, C, M, N, K, scale, true, dev, stream)
                    : run_bf16<Bf16SingleStream>(A, B, C, M, N, K, scale, true, dev, stream);
+  if (!scaled_acc && cg == 2)
+    return run_bf16<Bf16PairStore>(A, B, C, M, N, K, 0.0f, false, dev, stream);
   return cg == 2 ? run_bf16<Bf16Pair>(A, B, C, M, N, K, scale, scaled_acc, dev, stream)
                  : run_bf16<Bf16Single>(A, B, C, M, N, K, scale, scaled_acc, dev, stream);
 }

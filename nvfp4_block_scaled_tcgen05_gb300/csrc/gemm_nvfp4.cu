@@ -4,21 +4,26 @@
 // layout" / "Layout semantics"), FP16 output.
 //
 // Each 256-element K stage carries, per 128 rows, the 4 consecutive 512-byte
-// scale atoms of that K range (2 KB, contiguous in the hardware layout);
-// they are TMA-loaded as one 256 x u64 box and tcgen05.cp'd into a per-stage
-// TMEM slot ahead of the stage's 4 MMAs.  One TMEM accumulator (256 columns)
-// plus the scale slots fill the 512 columns, so the epilogue is
-// register-staged: 8 warps read the whole accumulator, release it, then
-// convert and store while the next tile's MMAs run.
+// scale atoms of that K range (2 KB, contiguous in the hardware layout),
+// which tcgen05.cp moves into a per-stage TMEM slot ahead of the stage's 4
+// MMAs.  The MMA reads the scales of row 32*i + g from TMEM lane 32*i + g;
+// staging every atom four times in shared memory (one TMA box whose replica
+// dimension has stride 0) lets one 128-lane x 32-byte copy fill the scale
+// columns of two A atoms or of one MMA's two B atoms: 6 copies per stage
+// instead of 12, which the tensor pipe needs (measured 256 -> 201 us at
+// 4096 x 7168 x 16384).  One TMEM accumulator (256 columns) plus the scale
+// slots fill the 512 columns, so the epilogue is register-staged: 8 warps
+// read the whole accumulator, release it, then convert and store straight
+// to global memory while the next tile's MMAs run.
 //
 // Configurations: pair (cta_group::2, 256 x 256 tiles, each CTA stages its
-// 128 A rows, 128 B rows and the scales of all 256 B rows, 5 stages) and
+// 128 A rows, 128 B rows and the scales of all 256 B rows, 4 stages) and
 // single (cta_group::1, 128 x 256 tiles, 3 stages) for small problems.
 #include "launch.cuh"
 
 namespace gb300 {
 
-using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 1>;
+using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 4, 8, 0, true, true>;
 using Nvfp4Single = TileCfg<Operand::kNVFP4, 1, 256, 3, 8, 1>;
 
 template <class Cfg>
@@ -36,12 +41,25 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
     rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c, uint64_t(N), uint64_t(M),
                         uint64_t(L), 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   // scales: one row of rest_k * 512 bytes (= rest_k * 64 u64) per (l, 128-row block)
+  if (rc == GEMM_OK) {
+    if constexpr (Cfg::SFA_REP) {
+      // [atom][replica][64 u64]: the replica dimension has stride 0, so one
+      // box of 4 x 4 x 512 B stages each of a stage's 4 atoms four times.
+      rc = encode_tmap_3d_strided(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT64, sfa, 64, 4,
+                                  uint64_t(L) * rest_m * rest_k, 0, 512, 64, 4, 4,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      rc = encode_tmap_3d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sfa, uint64_t(rest_k) * 64,
+                          uint64_t(L) * rest_m, 1, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+  }
   if (rc == GEMM_OK)
-    rc = encode_tmap_3d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sfa, uint64_t(rest_k) * 64,
-                        uint64_t(L) * rest_m, 1, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (rc == GEMM_OK)
-    rc = encode_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sfb, uint64_t(rest_k) * 64,
-                        uint64_t(L) * rest_n, 1, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    rc = Cfg::SFB_REP
+             ? encode_tmap_3d_strided(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT64, sfb, 64, 4,
+                                      uint64_t(L) * rest_n * rest_k, 0, 512, 64, 4, 4,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE)
+             : encode_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, sfb, uint64_t(rest_k) * 64,
+                              uint64_t(L) * rest_n, 1, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != GEMM_OK) return rc;
   GemmParams p{};
   p.M = M;
@@ -57,6 +75,7 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
   p.rest_m = rest_m;
   p.rest_n = rest_n;
   p.rest_k = rest_k;
+  p.c_ptr = c;
   p.status = dev.status;
   p.timeout_ns = wait_timeout_ns();
   return launch_tcgen05<Cfg, Epilogue::kStoreFP16>(ta, tb, tc, tsa, tsb, p, dev, stream);

@@ -34,6 +34,12 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, 
                    uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
                    CUtensorMapSwizzle swizzle);
 
+// Same, with explicit byte strides of dimensions 1 and 2 and a full 3-D box.
+int encode_tmap_3d_strided(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                           uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                           uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                           CUtensorMapSwizzle swizzle);
+
 // Launchers; arguments are validated by the caller.
 int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
                      bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream);

@@ -46,11 +46,13 @@ struct GemmParams {
   int k_splits, kb_per_split;     // split-K: the batch index l selects K blocks
                                   // [l*kb_per_split, (l+1)*kb_per_split); 1 / num_k_blocks otherwise
   float scale;                    // scaled-acc factor
+  void* c_ptr;                    // output base (direct-store epilogue only)
   unsigned int* status;           // device status word
   unsigned long long timeout_ns;  // bound on every wait
 };
 
-template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2>
+template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
+          bool SFA_REP_ = true, bool SFB_REP_ = false>
 struct TileCfg {
   static constexpr Operand kOp = OP;
   static constexpr bool kFP4 = (OP == Operand::kNVFP4);
@@ -72,11 +74,24 @@ struct TileCfg {
   static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int SF_ATOM = 512;             // 128 rows x 4 scales
   static constexpr int SFB_ATOMS = kFP4 ? BN / 128 : 0;  // every CTA holds the scales of all BN rows of B
-  static constexpr int SFA_BYTES = kFP4 ? KSTEPS * SF_ATOM : 0;
-  static constexpr int SFB_BYTES = kFP4 ? SFB_ATOMS * KSTEPS * SF_ATOM : 0;
+  // NVFP4 scale staging for A.  The block-scaled MMA reads the four scales
+  // of row 32*i + g from TMEM lane 32*i + g, column base + i; the replicating
+  // 32x128b copy writes every 512-byte atom into all four lane quarters.
+  // With SFA_REP each atom is instead staged four times in shared memory
+  // (one replica per lane quarter) so that one 128-lane x 32-byte copy fills
+  // the scale columns of two MMAs: 2 copies per stage instead of 4 (the
+  // tensor pipe slows down sharply past ~10 copies per 4-MMA stage).
+  static constexpr bool SFA_REP = kFP4 && SFA_REP_;
+  static constexpr int SFA_BYTES = kFP4 ? KSTEPS * SF_ATOM * (SFA_REP ? 4 : 1) : 0;
+  // SFB_REP: the same for B: per MMA, the 2 atoms of a 256-row B tile are
+  // staged 4 times each and one 128-lane x 32-byte copy fills its 8 columns.
+  static constexpr bool SFB_REP = kFP4 && SFB_REP_;
+  static_assert(!SFB_REP || SFB_ATOMS == 2, "replicated B scales assume a 256-row B tile");
+  static constexpr int SFB_ATOM_BYTES = kFP4 ? KSTEPS * SF_ATOM * (SFB_REP ? 4 : 1) : 0;  // per B atom
+  static constexpr int SFB_BYTES = SFB_ATOMS * SFB_ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int EPI_BOX_BYTES = 32 * 128;  // 32 rows x 64 16-bit values
-  static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BOX_BYTES;
+  static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BOX_BYTES;  // 0: direct stores
   // TMEM columns: accumulators first, then one scale slot per smem stage.
   static constexpr int SF_COLS = kFP4 ? KSTEPS * 4 * (1 + SFB_ATOMS) : 0;
   static constexpr int NUM_ACC = (2 * BN + STAGES * SF_COLS <= 512) ? 2 : 1;
@@ -195,6 +210,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // scaled-acc with two buffer halves per epilogue warp: prefetch the next tile
   constexpr bool kLookahead = (EPI == Epilogue::kScaledAccBF16) && !Cfg::kRegEpi &&
                               (Cfg::EPI_BUFS == 2 * (Cfg::EPI_COLS / 64));
+  // Without epilogue buffers the 16-bit outputs are written straight from
+  // registers with 16-byte global stores (frees shared memory for stages).
+  constexpr bool kDirectStore = (Cfg::EPI_BUFS == 0);
+  static_assert(!kDirectStore || EPI == Epilogue::kStoreBF16 || EPI == Epilogue::kStoreFP16,
+                "direct stores serve the plain 16-bit epilogues");
+  // L2 policy hints: keep the operands resident (they are re-read by other
+  // tiles), let the once-written output leave first.
+  constexpr bool kHintLoads = true;
+  constexpr bool kL2Hints = true;  // output stores
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -261,6 +285,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t pol_ab = ptx::policy_evict_last();
+      (void)pol_ab;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // bit s: stage s has a load in flight / its parity
@@ -273,7 +299,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int sfb_atoms = 0;
         if constexpr (kFP4) sfb_atoms = min(Cfg::SFB_ATOMS, p.rest_n - nb * Cfg::SFB_ATOMS);
         const uint32_t tx = uint32_t(CG) * (Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES +
-                                            uint32_t(sfb_atoms) * Cfg::KSTEPS * Cfg::SF_ATOM);
+                                            uint32_t(sfb_atoms) * Cfg::SFB_ATOM_BYTES);
         // split-K: l is the split; A and B are then single 2-D tensors (z = 0)
         const int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
         const int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
@@ -286,26 +312,58 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), tx);
           if constexpr (CG == 1) {
             const uint32_t fb = full_bar(stage);
-            ptx::tma_load_3d(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l);
-            ptx::tma_load_3d(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l);
+            if constexpr (kHintLoads) {
+              ptx::tma_load_3d_hint(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l, pol_ab);
+              ptx::tma_load_3d_hint(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l, pol_ab);
+            } else {
+              ptx::tma_load_3d(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l);
+              ptx::tma_load_3d(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l);
+            }
             if constexpr (kFP4) {
               // 4 consecutive atoms (tile_k = 4kb .. 4kb+3) = 2 KB = 256 u64 per 128 rows
-              ptx::tma_load_3d(stage_sfa(stage), &tmap_sfa, fb, kb * 256, l * p.rest_m + mb, 0);
-              for (int at = 0; at < sfb_atoms; ++at)
-                ptx::tma_load_3d(stage_sfb(stage) + at * Cfg::KSTEPS * Cfg::SF_ATOM, &tmap_sfb, fb,
-                                 kb * 256, l * p.rest_n + nb * Cfg::SFB_ATOMS + at, 0);
+              if constexpr (Cfg::SFA_REP) {
+                // one box = the stage's 4 atoms, each 4 times ([atom][replica][512 B])
+                ptx::tma_load_3d(stage_sfa(stage), &tmap_sfa, fb, 0, 0,
+                                 (l * p.rest_m + mb) * p.rest_k + 4 * kb);
+              } else {
+                ptx::tma_load_3d(stage_sfa(stage), &tmap_sfa, fb, kb * 256, l * p.rest_m + mb, 0);
+              }
+              for (int at = 0; at < sfb_atoms; ++at) {
+                if constexpr (Cfg::SFB_REP)
+                  ptx::tma_load_3d(stage_sfb(stage) + at * Cfg::SFB_ATOM_BYTES, &tmap_sfb, fb, 0, 0,
+                                   (l * p.rest_n + nb * Cfg::SFB_ATOMS + at) * p.rest_k + 4 * kb);
+                else
+                  ptx::tma_load_3d(stage_sfb(stage) + at * Cfg::KSTEPS * Cfg::SF_ATOM, &tmap_sfb,
+                                   fb, kb * 256, l * p.rest_n + nb * Cfg::SFB_ATOMS + at, 0);
+              }
             }
           } else {
             const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // the leader's barrier
-            ptx::tma_load_3d_pair(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l);
-            ptx::tma_load_3d_pair(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l);
+            if constexpr (kHintLoads) {
+              ptx::tma_load_3d_pair_hint(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l, pol_ab);
+              ptx::tma_load_3d_pair_hint(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l, pol_ab);
+            } else {
+              ptx::tma_load_3d_pair(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l);
+              ptx::tma_load_3d_pair(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l);
+            }
             if constexpr (kFP4) {
-              ptx::tma_load_3d_pair(stage_sfa(stage), &tmap_sfa, fb, kb * 256,
-                                    l * p.rest_m + mb * CG + int(rank), 0);
-              for (int at = 0; at < sfb_atoms; ++at)
-                ptx::tma_load_3d_pair(stage_sfb(stage) + at * Cfg::KSTEPS * Cfg::SF_ATOM,
-                                      &tmap_sfb, fb, kb * 256,
-                                      l * p.rest_n + nb * Cfg::SFB_ATOMS + at, 0);
+              if constexpr (Cfg::SFA_REP) {
+                ptx::tma_load_3d_pair(stage_sfa(stage), &tmap_sfa, fb, 0, 0,
+                                      (l * p.rest_m + mb * CG + int(rank)) * p.rest_k + 4 * kb);
+              } else {
+                ptx::tma_load_3d_pair(stage_sfa(stage), &tmap_sfa, fb, kb * 256,
+                                      l * p.rest_m + mb * CG + int(rank), 0);
+              }
+              for (int at = 0; at < sfb_atoms; ++at) {
+                if constexpr (Cfg::SFB_REP)
+                  ptx::tma_load_3d_pair(
+                      stage_sfb(stage) + at * Cfg::SFB_ATOM_BYTES, &tmap_sfb, fb, 0, 0,
+                      (l * p.rest_n + nb * Cfg::SFB_ATOMS + at) * p.rest_k + 4 * kb);
+                else
+                  ptx::tma_load_3d_pair(stage_sfb(stage) + at * Cfg::KSTEPS * Cfg::SF_ATOM,
+                                        &tmap_sfb, fb, kb * 256,
+                                        l * p.rest_n + nb * Cfg::SFB_ATOMS + at, 0);
+              }
             }
           }
           armed |= 1u << stage;
@@ -331,6 +389,45 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = Cfg::idesc();
+      // NVFP4: each stage's scale atoms go into that stage's TMEM slot right
+      // before the stage's MMAs (tcgen05.cp and tcgen05.mma from one thread
+      // execute in order).  Copying the next stage's scales ahead of this
+      // stage's MMAs measured slower on GB300 (the copies then sit in front
+      // of MMAs that could run).
+      auto copy_scales = [&](int s) {
+        if constexpr (kFP4) {
+          const uint32_t sfa_t = tmem_base + uint32_t(Cfg::SF_TMEM_BASE + s * Cfg::SF_COLS);
+          const uint32_t sfb_t = sfa_t + Cfg::KSTEPS * 4;
+          if constexpr (Cfg::SFA_REP) {
+            // replicas of atoms 2h and 2h+1 -> lanes 0..127, columns 8h .. 8h+7
+#pragma unroll
+            for (int h = 0; h < Cfg::KSTEPS / 2; ++h)
+              ptx::tc_cp_128x256b<CG>(
+                  sfa_t + 8 * h,
+                  ptx::smem_desc(stage_sfa(s) + 8 * h * Cfg::SF_ATOM, 4 * Cfg::SF_ATOM, 128, 0));
+          }
+          if constexpr (Cfg::SFB_REP) {
+            // per MMA j: replicas of B atom 0 (columns +0..3) and atom 1 (+4..7)
+#pragma unroll
+            for (int j = 0; j < Cfg::KSTEPS; ++j)
+              ptx::tc_cp_128x256b<CG>(
+                  sfb_t + 8 * j,
+                  ptx::smem_desc(stage_sfb(s) + 4 * j * Cfg::SF_ATOM, Cfg::SFB_ATOM_BYTES, 128, 0));
+          }
+#pragma unroll
+          for (int j = 0; j < Cfg::KSTEPS; ++j) {
+            if constexpr (!Cfg::SFA_REP)
+              ptx::tc_cp_32x128b_warpx4<CG>(
+                  sfa_t + 4 * j, ptx::smem_desc(stage_sfa(s) + j * Cfg::SF_ATOM, 0, 128, 0));
+            if constexpr (!Cfg::SFB_REP)
+#pragma unroll
+            for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
+              ptx::tc_cp_32x128b_warpx4<CG>(
+                  sfb_t + j * 4 * Cfg::SFB_ATOMS + 4 * at,
+                  ptx::smem_desc(stage_sfb(s) + (at * Cfg::KSTEPS + j) * Cfg::SF_ATOM, 0, 128, 0));
+          }
+        }
+      };
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -353,22 +450,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
+          // (the full barrier orders the TMA data before these MMAs; no
+          // tcgen05 fence is needed per stage)
           const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
           if constexpr (kFP4) {
+            copy_scales(stage);
             const uint32_t sfa_t = tmem_base + uint32_t(Cfg::SF_TMEM_BASE + stage * Cfg::SF_COLS);
             const uint32_t sfb_t = sfa_t + Cfg::KSTEPS * 4;
-#pragma unroll
-            for (int j = 0; j < Cfg::KSTEPS; ++j) {
-              ptx::tc_cp_32x128b_warpx4<CG>(
-                  sfa_t + 4 * j, ptx::smem_desc(stage_sfa(stage) + j * Cfg::SF_ATOM, 0, 128, 0));
-#pragma unroll
-              for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
-                ptx::tc_cp_32x128b_warpx4<CG>(
-                    sfb_t + j * 4 * Cfg::SFB_ATOMS + 4 * at,
-                    ptx::smem_desc(stage_sfb(stage) + (at * Cfg::KSTEPS + j) * Cfg::SF_ATOM, 0, 128,
-                                   0));
-            }
 #pragma unroll
             for (int j = 0; j < Cfg::KSTEPS; ++j)
               ptx::mma_nvf4<CG>(d_tmem, ptx::sw128_kmajor_desc(a0 + 32 * j),
@@ -408,6 +496,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // the leader CTA's acc_empty barriers (the MMA issuer waits on those)
     const uint32_t ae_leader0 = (CG == 2) ? ptx::mapa_shared(acc_empty(0), 0) : acc_empty(0);
     const uint32_t ae_leader1 = (CG == 2) ? ptx::mapa_shared(acc_empty(1), 0) : acc_empty(1);
+    const uint64_t pol_c = ptx::policy_evict_first();
+    (void)pol_c;
+    auto store_box = [&](uint32_t sbuf, int col0, int row0, int l) {
+      if constexpr (kL2Hints) ptx::tma_store_3d_hint(&tmap_c, sbuf, col0, row0, l, pol_c);
+      else ptx::tma_store_3d(&tmap_c, sbuf, col0, row0, l);
+    };
     uint32_t chunk_ctr = 0;
     uint32_t epi_parity = 0;     // bit b: parity of the next wait on epi_bar(e, b)
     uint32_t epi_pending = 0;    // bit b: a load into buffer b has not been waited for
@@ -475,6 +569,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 2 * NCH; ++i) ptx::tmem_ld_wait_regs(r[i]);
         release_acc(acc);
+        if constexpr (kDirectStore) {
+          const int grow = row0 + lane;
+          if (grow < p.M) {
+            uint16_t* dst = static_cast<uint16_t*>(p.c_ptr) +
+                            (size_t(l) * p.M + size_t(grow)) * size_t(p.N) + nb * BN + col_base;
+#pragma unroll
+            for (int i = 0; i < 2 * NCH; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (nb * BN + col_base + 32 * i + 8 * j < p.N)
+                  *reinterpret_cast<uint4*>(dst + 32 * i + 8 * j) =
+                      epi_chunk<EPI>(&r[i][8 * j], make_uint4(0, 0, 0, 0), 0.0f);
+          }
+        } else
 #pragma unroll
         for (int c = 0; c < NCH; ++c, ++chunk_ctr) {
           const int b = int(chunk_ctr % Cfg::EPI_BUFS);
@@ -491,7 +599,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmap_c, sbuf, col0, row0, l);
+            store_box(sbuf, col0, row0, l);
             ptx::bulk_commit_group();
           }
         }
@@ -527,7 +635,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmap_c, sbuf, col0, row0, l);
+            store_box(sbuf, col0, row0, l);
             ptx::bulk_commit_group();
           }
         }
@@ -550,8 +658,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmap_c, sbuf, col0, row0, l);
+            store_box(sbuf, col0, row0, l);
             ptx::bulk_commit_group();
+          }
+        }
+      } else if constexpr (kDirectStore) {
+        // 64 columns per chunk: each lane converts its row and writes eight
+        // 16-byte pieces straight to global memory (N % 8 == 0, so a piece
+        // is either wholly inside the matrix or wholly outside).
+        const int grow = row0 + lane;
+#pragma unroll 1
+        for (int c = 0; c < Cfg::EPI_COLS / 64; ++c) {
+          const int col0 = nb * BN + col_base + c * 64;
+          uint32_t r0[32], r1[32];
+          const uint32_t taddr = tacc + uint32_t(c * 64);
+          ptx::tmem_ld_32x32b_x32(taddr, r0);
+          ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
+          ptx::tmem_ld_wait_regs(r0);
+          ptx::tmem_ld_wait_regs(r1);
+          if (c == Cfg::EPI_COLS / 64 - 1) release_acc(acc);
+          if (grow >= p.M || col0 >= p.N) continue;
+          uint16_t* dst = static_cast<uint16_t*>(p.c_ptr) +
+                          (size_t(l) * p.M + size_t(grow)) * size_t(p.N) + col0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (col0 + 8 * j >= p.N) break;
+            const uint32_t* v = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
+            const uint4 o = epi_chunk<EPI>(v, make_uint4(0, 0, 0, 0), 0.0f);
+            *reinterpret_cast<uint4*>(dst + 8 * j) = o;
           }
         }
       } else {
@@ -592,7 +726,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmap_c, sbuf, col0, row0, l);
+            store_box(sbuf, col0, row0, l);
             ptx::bulk_commit_group();
           }
         }
