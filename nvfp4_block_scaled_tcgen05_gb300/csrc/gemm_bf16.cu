@@ -13,13 +13,18 @@
 // output of the next tile streams in while the current tile is written.
 // The MMA sequence of a tile does not depend on the stage count, so every
 // configuration with the same CTA group produces the same accumulators.
+#include <cstdlib>
+
 #include "launch.cuh"
 
 namespace gb300 {
 
 using Bf16Pair = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;
 using Bf16Single = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2>;
-using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;    // plain BF16 output
+// plain BF16 output: 128-deep stages (8 MMAs per stage), 3 stages
+using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 1, 2>;
+// two pairs per cluster sharing (multicasting) their A rows
+using Bf16PairMC = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2, true, false, 2>;
 using Bf16PairStream = TileCfg<Operand::kBF16, 2, 256, 3, 4, 8>;
 using Bf16SingleStream = TileCfg<Operand::kBF16, 1, 256, 2, 4, 8>;
 constexpr int kStreamMaxK = 256;  // scaled-acc K up to this uses the streaming configurations
@@ -29,7 +34,7 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
                     bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
   CUtensorMap ta, tb, tc;
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
-                          64, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+                          64, Cfg::A_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(K), uint64_t(N), 1,
                         64, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -45,7 +50,7 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
   p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
-  p.total_tiles = p.num_m_blocks * p.num_n_blocks;
+  p.total_tiles = p.num_m_blocks * ((p.num_n_blocks + Cfg::MC - 1) / Cfg::MC);
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blocks;
   p.scale = scale;
@@ -123,8 +128,15 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   if (scaled_acc && K <= kStreamMaxK)
     return cg == 2 ? run_bf16<Bf16PairStream>(A, B, C, M, N, K, scale, true, dev, stream)
                    : run_bf16<Bf16SingleStream>(A, B, C, M, N, K, scale, true, dev, stream);
-  if (!scaled_acc && cg == 2)
+  if (!scaled_acc && cg == 2) {
+    // GB300GEMM_MC=2 selects the A-multicast cluster; measured no faster
+    // than the plain pair on the shapes here (GB300), so it is opt-in.
+    const char* e = std::getenv("GB300GEMM_MC");
+    const bool mc = e && std::atoi(e) == 2;
+    if (mc && (N + 255) / 256 >= 2)
+      return run_bf16<Bf16PairMC>(A, B, C, M, N, K, 0.0f, false, dev, stream);
     return run_bf16<Bf16PairStore>(A, B, C, M, N, K, 0.0f, false, dev, stream);
+  }
   return cg == 2 ? run_bf16<Bf16Pair>(A, B, C, M, N, K, scale, scaled_acc, dev, stream)
                  : run_bf16<Bf16Single>(A, B, C, M, N, K, scale, scaled_acc, dev, stream);
 }

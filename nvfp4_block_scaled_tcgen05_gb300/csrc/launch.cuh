@@ -1,6 +1,6 @@
 // Host-side launch of tcgen05_gemm_kernel instantiations: one-time per-device
 // attributes, co-resident cluster count, cudaLaunchKernelEx with the cluster
-// dimension of the CTA group.
+// dimension of the configuration (CTA group x pairs sharing A).
 #pragma once
 
 #include <algorithm>
@@ -31,7 +31,7 @@ int launch_tcgen05(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = Cfg::CG;
+  attr[0].val.clusterDim.x = Cfg::CLUSTER;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(Cfg::THREADS);
@@ -45,16 +45,16 @@ int launch_tcgen05(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
         cudaSuccess)
       return GEMM_ERR_LAUNCH;
     int n = 0;
-    cfg.gridDim = dim3(Cfg::CG * (dev.num_sms / Cfg::CG));
+    cfg.gridDim = dim3(Cfg::CLUSTER * (dev.num_sms / Cfg::CLUSTER));
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
-      n = dev.num_sms / Cfg::CG;
+      n = dev.num_sms / Cfg::CLUSTER;
     }
-    clusters_cap = std::min(n, dev.num_sms / Cfg::CG);
+    clusters_cap = std::min(n, dev.num_sms / Cfg::CLUSTER);
     max_clusters[d].store(clusters_cap);
   }
   const int clusters = std::min(p.total_tiles, clusters_cap);
-  cfg.gridDim = dim3(clusters * Cfg::CG);
+  cfg.gridDim = dim3(clusters * Cfg::CLUSTER);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tsfa, tsfb, p);
   if (e != cudaSuccess) {
     cudaGetLastError();

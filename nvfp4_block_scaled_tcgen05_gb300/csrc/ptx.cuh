@@ -50,6 +50,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: true if the phase with parity `parity` has completed.
+// Unlike try_wait it never suspends the thread, so it can be issued between
+// MMAs without holding up the next issue.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -178,6 +193,18 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* 
       : "memory");
 }
 
+// Pair load multicast to the CTAs of `mask`: the box lands at the same
+// offset in each of them, and each one's pair leader is signalled on the
+// barrier at `bar`'s offset (`bar` addresses this CTA's pair leader).
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar,
+                                                    int x, int y, int z, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // CG is the CTA group: 1 (one SM) or 2 (a CTA pair sharing each MMA).
 template <int CG>
@@ -220,9 +247,10 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // Arrive (once) on an mbarrier when every tcgen05 operation this thread
 // issued before has completed.  With CG == 2 the arrive is multicast to the
-// barrier at the same offset in both CTAs of the pair.
+// barrier at the same offset in every CTA of `mask` (cluster ranks; the
+// default is the pair of a two-CTA cluster).
 template <int CG>
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
+__device__ __forceinline__ void tc_commit(uint32_t bar, uint16_t mask = 3) {
   if constexpr (CG == 1)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      bar)
@@ -231,7 +259,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(bar),
-        "h"(static_cast<uint16_t>(3))
+        "h"(mask)
         : "memory");
 }
 

@@ -52,11 +52,17 @@ struct GemmParams {
 };
 
 template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
-          bool SFA_REP_ = true, bool SFB_REP_ = false>
+          bool SFA_REP_ = true, bool SFB_REP_ = false, int MC_ = 1, int KSUB_ = 1>
 struct TileCfg {
   static constexpr Operand kOp = OP;
   static constexpr bool kFP4 = (OP == Operand::kNVFP4);
   static constexpr int CG = CG_;                  // CTAs per MMA (1 or 2)
+  // MC = 2: a cluster of two CTA pairs computes two horizontally adjacent
+  // tiles that share their A rows.  Each CTA loads half of its 128 A rows
+  // and multicasts them to the CTA with the same role in the other pair, so
+  // the L2 serves every A byte once per cluster instead of once per pair.
+  static constexpr int MC = MC_;
+  static constexpr int CLUSTER = CG * MC;         // CTAs per cluster
   static constexpr int BM = 128;                  // A rows / TMEM lanes per CTA
   static constexpr int TILE_M = BM * CG;          // C rows per tile
   static constexpr int BN = BN_;                  // C columns per tile (MMA N)
@@ -66,12 +72,19 @@ struct TileCfg {
   static constexpr int EPI_BUFS = EPI_BUFS_;
   static constexpr bool kRegEpi = (EPI_WARPS == 8);
   static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue warp
-  static constexpr int BK = kFP4 ? 256 : 64;      // K elements per stage = 128 bytes per row
-  static constexpr int KX = kFP4 ? 128 : 64;      // TMA x-extent per stage (bytes or elements)
+  // KSUB = 2 (BF16): a stage holds two 64-deep K sub-tiles per operand (two
+  // TMA boxes each), i.e. 8 MMAs per stage.  The per-stage work of the MMA
+  // issuer (barrier probe, release commit, bookkeeping) then has 1024 pipe
+  // cycles to hide behind instead of 512.
+  static constexpr int KSUB = KSUB_;
+  static constexpr int BK = kFP4 ? 256 : 64 * KSUB;  // K elements per stage
+  static constexpr int KX = kFP4 ? 128 : 64;      // TMA x-extent per sub-tile (bytes or elements)
   static constexpr int MMA_K = kFP4 ? 64 : 16;    // K per MMA = 32 bytes per row
   static constexpr int KSTEPS = BK / MMA_K;       // 4 MMAs per stage
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int A_SUB_BYTES = BM * 128;      // one 128-byte-wide K sub-tile
+  static constexpr int B_SUB_BYTES = B_ROWS * 128;
+  static constexpr int A_BYTES = A_SUB_BYTES * KSUB;
+  static constexpr int B_BYTES = B_SUB_BYTES * KSUB;
   static constexpr int SF_ATOM = 512;             // 128 rows x 4 scales
   static constexpr int SFB_ATOMS = kFP4 ? BN / 128 : 0;  // every CTA holds the scales of all BN rows of B
   // NVFP4 scale staging for A.  The block-scaled MMA reads the four scales
@@ -100,6 +113,12 @@ struct TileCfg {
   static_assert(NUM_ACC * BN + STAGES * SF_COLS <= TMEM_COLS, "TMEM column budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(CG == 1 || CG == 2, "CTA group");
+  static_assert(MC == 1 || (MC == 2 && CG == 2 && !kFP4), "A multicast: BF16 CTA pairs only");
+  static_assert(KSUB == 1 || (KSUB == 2 && !kFP4), "K sub-tiles: BF16 only");
+  static constexpr int A_SLICE_ROWS = BM / MC;    // A rows each CTA loads per stage
+  static constexpr int A_SLICE_BYTES = A_SLICE_ROWS * 128;
+  // the MMA issuer releases a stage only after the next stage's first MMA
+  static_assert(STAGES >= 2, "at least two pipeline stages");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA");
   static_assert(!kFP4 || BN % 128 == 0, "NVFP4 BN must cover whole 128-row scale atoms");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
@@ -125,19 +144,24 @@ struct TileCfg {
   }
 };
 
+// Cluster work item `tile` -> batch l, M block mb and this pair's N block
+// nb.  With MC pairs per cluster an item spans MC adjacent N blocks and pair
+// `pair` takes the pair-th (which may lie past N: the pair then still loads
+// and multiplies, for its partner's sake, but stores nothing).
 template <class Cfg>
-__device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int& l, int& mb,
-                                            int& nb) {
-  const int per_batch = p.num_m_blocks * p.num_n_blocks;
+__device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int pair, int& l,
+                                            int& mb, int& nb) {
+  const int n_items = (p.num_n_blocks + Cfg::MC - 1) / Cfg::MC;
+  const int per_batch = p.num_m_blocks * n_items;
   l = tile / per_batch;
   const int t = tile - l * per_batch;
-  const int group_tiles = Cfg::GROUP_M * p.num_n_blocks;
+  const int group_tiles = Cfg::GROUP_M * n_items;
   const int g = t / group_tiles;
   const int first_m = g * Cfg::GROUP_M;
   const int gm = min(p.num_m_blocks - first_m, Cfg::GROUP_M);
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
-  nb = r / gm;
+  nb = (r / gm) * Cfg::MC + pair;
 }
 
 // Converts 8 accumulator columns (v[0..7], FP32 bits) of one row and the
@@ -243,15 +267,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
-  const bool leader = (rank == 0);
-  const int cluster_id = blockIdx.x / CG;
-  const int num_clusters = gridDim.x / CG;
+  constexpr int MC = Cfg::MC;
+  const uint32_t rank = (Cfg::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;
+  const uint32_t peer = (CG == 2) ? (rank & 1u) : 0u;  // role within the CTA pair
+  const int pair = int(rank) / CG;                     // pair index within the cluster
+  const uint32_t pair_leader = rank & ~1u;             // rank of this pair's MMA issuer
+  const bool leader = (peer == 0);
+  const int cluster_id = blockIdx.x / Cfg::CLUSTER;
+  const int num_clusters = gridDim.x / Cfg::CLUSTER;
+  // tcgen05.commit targets: this pair's two CTAs; stage releases go to every
+  // CTA whose producer writes into this pair's shared memory (all of them)
+  const uint16_t pair_mask = uint16_t(3u << pair_leader);
+  const uint16_t release_mask = (MC == 2) ? uint16_t(0xF) : pair_mask;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), MC);  // one release per pair reading the stage
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(acc_full(b), 1);
@@ -277,7 +309,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     ptx::tmem_relinquish<CG>();
   }
   ptx::tc_fence_before();
-  if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+  if constexpr (Cfg::CLUSTER > 1) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Watch w{abort_flag, p.status, p.timeout_ns};
@@ -293,9 +325,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       bool ok = true;
       for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters) {
         int l, mb, nb;
-        decode_tile<Cfg>(tile, p, l, mb, nb);
-        const int a_row = mb * Cfg::TILE_M + int(rank) * Cfg::BM;
-        const int b_row = nb * BN + int(rank) * Cfg::B_ROWS;
+        decode_tile<Cfg>(tile, p, pair, l, mb, nb);
+        const int a_row = mb * Cfg::TILE_M + int(peer) * Cfg::BM;
+        const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
         int sfb_atoms = 0;
         if constexpr (kFP4) sfb_atoms = min(Cfg::SFB_ATOMS, p.rest_n - nb * Cfg::SFB_ATOMS);
         const uint32_t tx = uint32_t(CG) * (Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES +
@@ -312,12 +344,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), tx);
           if constexpr (CG == 1) {
             const uint32_t fb = full_bar(stage);
-            if constexpr (kHintLoads) {
-              ptx::tma_load_3d_hint(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l, pol_ab);
-              ptx::tma_load_3d_hint(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l, pol_ab);
-            } else {
-              ptx::tma_load_3d(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l);
-              ptx::tma_load_3d(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l);
+#pragma unroll
+            for (int sub = 0; sub < Cfg::KSUB; ++sub) {
+              const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
+              const uint32_t da = stage_a(stage) + sub * Cfg::A_SUB_BYTES;
+              const uint32_t db = stage_b(stage) + sub * Cfg::B_SUB_BYTES;
+              if constexpr (kHintLoads) {
+                ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
+                ptx::tma_load_3d_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
+              } else {
+                ptx::tma_load_3d(da, &tmap_a, fb, x, a_row, l);
+                ptx::tma_load_3d(db, &tmap_b, fb, x, b_row, l);
+              }
             }
             if constexpr (kFP4) {
               // 4 consecutive atoms (tile_k = 4kb .. 4kb+3) = 2 KB = 256 u64 per 128 rows
@@ -338,21 +376,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               }
             }
           } else {
-            const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // the leader's barrier
-            if constexpr (kHintLoads) {
-              ptx::tma_load_3d_pair_hint(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l, pol_ab);
-              ptx::tma_load_3d_pair_hint(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l, pol_ab);
-            } else {
-              ptx::tma_load_3d_pair(stage_a(stage), &tmap_a, fb, kb * Cfg::KX, a_row, l);
-              ptx::tma_load_3d_pair(stage_b(stage), &tmap_b, fb, kb * Cfg::KX, b_row, l);
+            const uint32_t fb = ptx::mapa_shared(full_bar(stage), pair_leader);  // the leader's barrier
+#pragma unroll
+            for (int sub = 0; sub < Cfg::KSUB; ++sub) {
+              const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
+              const uint32_t da = stage_a(stage) + sub * Cfg::A_SUB_BYTES;
+              const uint32_t db = stage_b(stage) + sub * Cfg::B_SUB_BYTES;
+              if constexpr (MC == 2) {
+                // this CTA's half of the shared A rows, to both pairs
+                const uint16_t a_mask = uint16_t((1u << peer) | (1u << (2 + peer)));
+                ptx::tma_load_3d_pair_mc(da + pair * Cfg::A_SLICE_BYTES, &tmap_a, fb, x,
+                                         a_row + pair * Cfg::A_SLICE_ROWS, l, a_mask);
+                ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
+              } else if constexpr (kHintLoads) {
+                ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
+                ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
+              } else {
+                ptx::tma_load_3d_pair(da, &tmap_a, fb, x, a_row, l);
+                ptx::tma_load_3d_pair(db, &tmap_b, fb, x, b_row, l);
+              }
             }
             if constexpr (kFP4) {
               if constexpr (Cfg::SFA_REP) {
                 ptx::tma_load_3d_pair(stage_sfa(stage), &tmap_sfa, fb, 0, 0,
-                                      (l * p.rest_m + mb * CG + int(rank)) * p.rest_k + 4 * kb);
+                                      (l * p.rest_m + mb * CG + int(peer)) * p.rest_k + 4 * kb);
               } else {
                 ptx::tma_load_3d_pair(stage_sfa(stage), &tmap_sfa, fb, kb * 256,
-                                      l * p.rest_m + mb * CG + int(rank), 0);
+                                      l * p.rest_m + mb * CG + int(peer), 0);
               }
               for (int at = 0; at < sfb_atoms; ++at) {
                 if constexpr (Cfg::SFB_REP)
@@ -428,62 +478,113 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
         }
       };
+      // The tensor pipe accepts the next MMA only about one MMA ahead of
+      // the one executing, so thread work between a stage's last MMA and
+      // the next stage's first MMA leaves the pipe idle.  The issuer walks
+      // the flat sequence of (tile, K block) jobs and keeps that gap short:
+      // the next stage's full barrier is probed (non-blocking) between this
+      // stage's MMAs, a stage is released by a commit placed after the next
+      // stage's first MMA (the commit then also waits for that MMA, which
+      // only delays the release a little), and the smem descriptors are
+      // stage-0 descriptors plus an offset.
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters, ++it) {
-        const int acc = it % Cfg::NUM_ACC;
-        const uint32_t acc_phase = uint32_t(it / Cfg::NUM_ACC) & 1u;
-        if (!wait_bar(acc_empty(acc), acc_phase ^ 1u, w, 2)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+      int tile = cluster_id;
+      int pending_empty = -1;  // stage whose release commit is still to be issued
+      // K tail: the last K block may need fewer than KSTEPS MMAs (the
+      // zero-filled rest of its stage needs none)
+      const int tail_kb = (p.K % Cfg::BK) ? p.K / Cfg::BK : -1;
+      const int tail_steps = (p.K % Cfg::BK + Cfg::MMA_K - 1) / Cfg::MMA_K;
+      if (tile < p.total_tiles) {
         int l, mb, nb;
-        decode_tile<Cfg>(tile, p, l, mb, nb);
-        const int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
-        const int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!wait_bar(full_bar(stage), phase, w, 3)) {
-            ok = false;
-            break;
+        decode_tile<Cfg>(tile, p, pair, l, mb, nb);
+        int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
+        int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
+        int kb = kb_begin;
+        int acc = 0;
+        ok = wait_bar(acc_empty(0), 1u, w, 2) && wait_bar(full_bar(0), 0u, w, 3);
+        ptx::tc_fence_after();
+        // Stage s, MMA j: start address + s * STAGE_BYTES + 32 j, i.e. the
+        // 14-bit start field (address >> 4) grows by that >> 4; shared
+        // addresses stay below 2^18 bytes, so the field never carries over.
+        const uint64_t adesc0 = ptx::sw128_kmajor_desc(stage_a(0));
+        const uint64_t bdesc0 = ptx::sw128_kmajor_desc(stage_b(0));
+        while (ok) {
+          const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+          const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
+          const bool last_kb = (kb + 1 == kb_end);
+          const int next_tile = last_kb ? tile + num_clusters : tile;
+          const bool has_next = next_tile < p.total_tiles;
+          const int nstage = (stage + 1 == STAGES) ? 0 : stage + 1;
+          const uint32_t nphase = (stage + 1 == STAGES) ? (phase ^ 1u) : phase;
+          bool next_ready = true;
+          const int nsteps = (kb == tail_kb) ? tail_steps : Cfg::KSTEPS;
+          uint32_t sfa_t = 0, sfb_t = 0;
+          if constexpr (kFP4) {
+            copy_scales(stage);
+            sfa_t = tmem_base + uint32_t(Cfg::SF_TMEM_BASE + stage * Cfg::SF_COLS);
+            sfb_t = sfa_t + Cfg::KSTEPS * 4;
           }
           // (the full barrier orders the TMA data before these MMAs; no
           // tcgen05 fence is needed per stage)
-          const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
-          if constexpr (kFP4) {
-            copy_scales(stage);
-            const uint32_t sfa_t = tmem_base + uint32_t(Cfg::SF_TMEM_BASE + stage * Cfg::SF_COLS);
-            const uint32_t sfb_t = sfa_t + Cfg::KSTEPS * 4;
 #pragma unroll
-            for (int j = 0; j < Cfg::KSTEPS; ++j)
-              ptx::mma_nvf4<CG>(d_tmem, ptx::sw128_kmajor_desc(a0 + 32 * j),
-                                ptx::sw128_kmajor_desc(b0 + 32 * j), idesc, sfa_t + 4 * j,
-                                sfb_t + j * 4 * Cfg::SFB_ATOMS, (kb != kb_begin) || (j != 0));
-          } else {
-            // K tail: the zero-filled part of the last stage needs no MMA.
-            const int krem = p.K - kb * Cfg::BK;
-            const int nsteps = krem >= Cfg::BK ? Cfg::KSTEPS : (krem + Cfg::MMA_K - 1) / Cfg::MMA_K;
-#pragma unroll
-            for (int j = 0; j < Cfg::KSTEPS; ++j)
-              if (j < nsteps)
-                ptx::mma_bf16<CG>(d_tmem, ptx::sw128_kmajor_desc(a0 + 32 * j),
-                                  ptx::sw128_kmajor_desc(b0 + 32 * j), idesc,
-                                  (kb != kb_begin) || (j != 0));
+          for (int j = 0; j < Cfg::KSTEPS; ++j) {
+            if (j < nsteps) {
+              // step j: K sub-tile j / 4, 32-byte K slice j % 4 within it
+              const uint64_t ad =
+                  adesc0 + soff + uint64_t(((j / 4) * Cfg::A_SUB_BYTES + 32 * (j % 4)) >> 4);
+              const uint64_t bd =
+                  bdesc0 + soff + uint64_t(((j / 4) * Cfg::B_SUB_BYTES + 32 * (j % 4)) >> 4);
+              const uint32_t accum = (kb != kb_begin) || (j != 0);
+              if constexpr (kFP4)
+                ptx::mma_nvf4<CG>(d_tmem, ad, bd, idesc, sfa_t + 4 * j,
+                                  sfb_t + j * 4 * Cfg::SFB_ATOMS, accum);
+              else
+                ptx::mma_bf16<CG>(d_tmem, ad, bd, idesc, accum);
+            }
+            if (j == 0 && pending_empty >= 0)
+              ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
+            if (j == (Cfg::KSTEPS > 2 ? 1 : 0) && has_next)
+              next_ready = ptx::mbar_test_wait(full_bar(nstage), nphase);
           }
-          ptx::tc_commit<CG>(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (last_kb) {
+            // tile done: release the stage and hand the accumulator over now
+            ptx::tc_commit<CG>(empty_bar(stage), release_mask);
+            ptx::tc_commit<CG>(acc_full(acc), pair_mask);
+            pending_empty = -1;
+          } else {
+            pending_empty = stage;
+          }
+          if (!has_next) break;
+          stage = nstage;
+          phase = nphase;
+          if (last_kb) {
+            tile = next_tile;
+            ++it;
+            decode_tile<Cfg>(tile, p, pair, l, mb, nb);
+            kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
+            kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
+            kb = kb_begin;
+            acc = it % Cfg::NUM_ACC;
+            if (!wait_bar(acc_empty(acc), (uint32_t(it / Cfg::NUM_ACC) & 1u) ^ 1u, w, 2)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+          } else {
+            ++kb;
+          }
+          if (!next_ready && !wait_bar(full_bar(stage), phase, w, 3)) {
+            ok = false;
+            break;
           }
         }
-        if (!ok) break;
-        ptx::tc_commit<CG>(acc_full(acc));
+        if (pending_empty >= 0) ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
       }
       // Every MMA / copy issued must be complete before TMEM is released.
-      ptx::tc_commit<CG>(mma_done);
+      ptx::tc_commit<CG>(mma_done, pair_mask);
       drain_bar(mma_done, 0, w);
     }
   } else {
@@ -494,8 +595,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t lane_off = uint32_t(q * 32) << 16;
     const uint32_t buf0 = epi_base + e * Cfg::EPI_BUFS * Cfg::EPI_BOX_BYTES;
     // the leader CTA's acc_empty barriers (the MMA issuer waits on those)
-    const uint32_t ae_leader0 = (CG == 2) ? ptx::mapa_shared(acc_empty(0), 0) : acc_empty(0);
-    const uint32_t ae_leader1 = (CG == 2) ? ptx::mapa_shared(acc_empty(1), 0) : acc_empty(1);
+    const uint32_t ae_leader0 =
+        (CG == 2) ? ptx::mapa_shared(acc_empty(0), pair_leader) : acc_empty(0);
+    const uint32_t ae_leader1 =
+        (CG == 2) ? ptx::mapa_shared(acc_empty(1), pair_leader) : acc_empty(1);
     const uint64_t pol_c = ptx::policy_evict_first();
     (void)pol_c;
     auto store_box = [&](uint32_t sbuf, int col0, int row0, int l) {
@@ -520,8 +623,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if constexpr (kLookahead) {
         constexpr int NCH = Cfg::EPI_COLS / 64;
         int l2, mb2, nb2;
-        decode_tile<Cfg>(t, p, l2, mb2, nb2);
-        const int r0 = mb2 * Cfg::TILE_M + int(rank) * Cfg::BM + q * 32;
+        decode_tile<Cfg>(t, p, pair, l2, mb2, nb2);
+        const int r0 = mb2 * Cfg::TILE_M + int(peer) * Cfg::BM + q * 32;
         if (r0 >= p.M) return;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
@@ -541,7 +644,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters, ++it) {
       int l, mb, nb;
-      decode_tile<Cfg>(tile, p, l, mb, nb);
+      decode_tile<Cfg>(tile, p, pair, l, mb, nb);
       const int acc = it % Cfg::NUM_ACC;
       const uint32_t acc_phase = uint32_t(it / Cfg::NUM_ACC) & 1u;
       if constexpr (kLookahead) {
@@ -556,7 +659,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       ok = __all_sync(0xffffffffu, wait_bar(acc_full(acc), acc_phase, w, 4));
       if (!ok) break;
       ptx::tc_fence_after();
-      const int row0 = mb * Cfg::TILE_M + int(rank) * Cfg::BM + q * 32;
+      const int row0 = mb * Cfg::TILE_M + int(peer) * Cfg::BM + q * 32;
       const bool rows_live = row0 < p.M;
       const uint32_t tacc = tmem_base + lane_off + uint32_t(acc * BN + col_base);
 
@@ -742,7 +845,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   }
 
   ptx::tc_fence_before();
-  if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+  if constexpr (Cfg::CLUSTER > 1) ptx::cluster_sync(); else __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);

@@ -25,11 +25,14 @@ def g():
     assert lib.gemm_get_device_status() == 0
 
 
-@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
+@pytest.fixture(params=[(1, 1), (2, 1), (2, 2)], ids=["cta1", "cta2", "cta2x2"])
 def cg(request, monkeypatch):
-    """Force the single-CTA or the CTA-pair (cta_group::2) kernel."""
-    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(request.param))
-    return request.param
+    """Force the single-CTA kernel, the CTA-pair (cta_group::2) kernel, or
+    two CTA pairs per cluster sharing their A rows by TMA multicast."""
+    group, mc = request.param
+    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(group))
+    monkeypatch.setenv("GB300GEMM_MC", str(mc))
+    return group
 
 
 def amax(x):
