@@ -439,115 +439,136 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = Cfg::idesc();
-      // NVFP4: each stage's scale atoms go into that stage's TMEM slot right
-      // before the stage's MMAs (tcgen05.cp and tcgen05.mma from one thread
-      // execute in order).  Copying the next stage's scales ahead of this
-      // stage's MMAs measured slower on GB300 (the copies then sit in front
-      // of MMAs that could run).
-      auto copy_scales = [&](int s) {
+      // NVFP4: the scale atoms of MMA j of stage s go into the stage's TMEM
+      // slot right before that MMA (tcgen05.cp and tcgen05.mma from one
+      // thread execute in order).  Spread between the MMAs the copies
+      // overlap MMA execution; bunched in front of a stage's MMAs they held
+      // the tensor pipe near 70% of its FP4 rate on GB300 (90% interleaved).
+      // Descriptors and TMEM addresses of stage 0; stage s adds
+      // s * STAGE_BYTES >> 4 to a descriptor's start field (no carry, as
+      // for the operand descriptors) and s * SF_COLS to a TMEM column.
+      const uint32_t sf_t0 = tmem_base + uint32_t(Cfg::SF_TMEM_BASE);
+      uint64_t sfa_d0 = 0, sfb_d0 = 0;
+      if constexpr (kFP4) {
+        sfa_d0 = Cfg::SFA_REP ? ptx::smem_desc(stage_sfa(0), 4 * Cfg::SF_ATOM, 128, 0)
+                              : ptx::smem_desc(stage_sfa(0), 0, 128, 0);
+        sfb_d0 = Cfg::SFB_REP ? ptx::smem_desc(stage_sfb(0), Cfg::SFB_ATOM_BYTES, 128, 0)
+                              : ptx::smem_desc(stage_sfb(0), 0, 128, 0);
+      }
+      auto copy_scales_for = [&](uint32_t sfa_t, uint64_t soff, int j) {
         if constexpr (kFP4) {
-          const uint32_t sfa_t = tmem_base + uint32_t(Cfg::SF_TMEM_BASE + s * Cfg::SF_COLS);
           const uint32_t sfb_t = sfa_t + Cfg::KSTEPS * 4;
           if constexpr (Cfg::SFA_REP) {
-            // replicas of atoms 2h and 2h+1 -> lanes 0..127, columns 8h .. 8h+7
-#pragma unroll
-            for (int h = 0; h < Cfg::KSTEPS / 2; ++h)
-              ptx::tc_cp_128x256b<CG>(
-                  sfa_t + 8 * h,
-                  ptx::smem_desc(stage_sfa(s) + 8 * h * Cfg::SF_ATOM, 4 * Cfg::SF_ATOM, 128, 0));
+            // replicas of atoms j and j+1 -> lanes 0..127, columns 4j .. 4j+7
+            if (j % 2 == 0)
+              ptx::tc_cp_128x256b<CG>(sfa_t + 4 * j,
+                                      sfa_d0 + soff + uint64_t((4 * j * Cfg::SF_ATOM) >> 4));
+          } else {
+            ptx::tc_cp_32x128b_warpx4<CG>(sfa_t + 4 * j,
+                                          sfa_d0 + soff + uint64_t((j * Cfg::SF_ATOM) >> 4));
           }
           if constexpr (Cfg::SFB_REP) {
-            // per MMA j: replicas of B atom 0 (columns +0..3) and atom 1 (+4..7)
-#pragma unroll
-            for (int j = 0; j < Cfg::KSTEPS; ++j)
-              ptx::tc_cp_128x256b<CG>(
-                  sfb_t + 8 * j,
-                  ptx::smem_desc(stage_sfb(s) + 4 * j * Cfg::SF_ATOM, Cfg::SFB_ATOM_BYTES, 128, 0));
-          }
-#pragma unroll
-          for (int j = 0; j < Cfg::KSTEPS; ++j) {
-            if constexpr (!Cfg::SFA_REP)
-              ptx::tc_cp_32x128b_warpx4<CG>(
-                  sfa_t + 4 * j, ptx::smem_desc(stage_sfa(s) + j * Cfg::SF_ATOM, 0, 128, 0));
-            if constexpr (!Cfg::SFB_REP)
+            // replicas of B atom 0 (columns +0..3) and atom 1 (+4..7)
+            ptx::tc_cp_128x256b<CG>(sfb_t + 8 * j,
+                                    sfb_d0 + soff + uint64_t((4 * j * Cfg::SF_ATOM) >> 4));
+          } else {
 #pragma unroll
             for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
               ptx::tc_cp_32x128b_warpx4<CG>(
                   sfb_t + j * 4 * Cfg::SFB_ATOMS + 4 * at,
-                  ptx::smem_desc(stage_sfb(s) + (at * Cfg::KSTEPS + j) * Cfg::SF_ATOM, 0, 128, 0));
+                  sfb_d0 + soff + uint64_t(((at * Cfg::KSTEPS + j) * Cfg::SF_ATOM) >> 4));
           }
         }
       };
-      // The tensor pipe accepts the next MMA only about one MMA ahead of
-      // the one executing, so thread work between a stage's last MMA and
-      // the next stage's first MMA leaves the pipe idle.  The issuer walks
-      // the flat sequence of (tile, K block) jobs and keeps that gap short:
-      // the next stage's full barrier is probed (non-blocking) between this
-      // stage's MMAs, a stage is released by a commit placed after the next
-      // stage's first MMA (the commit then also waits for that MMA, which
-      // only delays the release a little), and the smem descriptors are
-      // stage-0 descriptors plus an offset.
+      // The tensor pipe holds little more than the MMA it is executing, so
+      // thread work between a stage's last MMA and the next stage's first
+      // MMA leaves it idle, and every tcgen05 instruction costs the issuing
+      // thread tens of cycles.  The issuer walks the flat sequence of
+      // (tile, K block) jobs and keeps that gap to a few instructions: the
+      // next job (tile decode, accumulator wait, a non-blocking probe of its
+      // full barrier) is prepared between this job's MMAs; a stage is
+      // released by a commit placed after the next stage's first MMA (the
+      // commit then also waits for that MMA, which only delays the release
+      // a little); smem descriptors are stage-0 descriptors plus an offset.
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int it = 0;
       int tile = cluster_id;
       int pending_empty = -1;  // stage whose release commit is still to be issued
       // K tail: the last K block may need fewer than KSTEPS MMAs (the
       // zero-filled rest of its stage needs none)
       const int tail_kb = (p.K % Cfg::BK) ? p.K / Cfg::BK : -1;
       const int tail_steps = (p.K % Cfg::BK + Cfg::MMA_K - 1) / Cfg::MMA_K;
+      constexpr int kPrep = Cfg::KSTEPS > 2 ? 1 : 0;  // MMA after which the next job is prepared
       if (tile < p.total_tiles) {
         int l, mb, nb;
         decode_tile<Cfg>(tile, p, pair, l, mb, nb);
         int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
         int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
         int kb = kb_begin;
-        int acc = 0;
+        int it = 0, acc = 0;
         ok = wait_bar(acc_empty(0), 1u, w, 2) && wait_bar(full_bar(0), 0u, w, 3);
         ptx::tc_fence_after();
-        // Stage s, MMA j: start address + s * STAGE_BYTES + 32 j, i.e. the
-        // 14-bit start field (address >> 4) grows by that >> 4; shared
+        // Stage s, MMA j: start address + s * STAGE_BYTES + offset of j, i.e.
+        // the 14-bit start field (address >> 4) grows by that >> 4; shared
         // addresses stay below 2^18 bytes, so the field never carries over.
         const uint64_t adesc0 = ptx::sw128_kmajor_desc(stage_a(0));
         const uint64_t bdesc0 = ptx::sw128_kmajor_desc(stage_b(0));
         while (ok) {
           const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
           const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
+          const uint32_t sfa_t = sf_t0 + uint32_t(stage * Cfg::SF_COLS);
+          const int nsteps = (kb == tail_kb) ? tail_steps : Cfg::KSTEPS;
+          const bool first_kb = (kb == kb_begin);
           const bool last_kb = (kb + 1 == kb_end);
-          const int next_tile = last_kb ? tile + num_clusters : tile;
-          const bool has_next = next_tile < p.total_tiles;
           const int nstage = (stage + 1 == STAGES) ? 0 : stage + 1;
           const uint32_t nphase = (stage + 1 == STAGES) ? (phase ^ 1u) : phase;
-          bool next_ready = true;
-          const int nsteps = (kb == tail_kb) ? tail_steps : Cfg::KSTEPS;
-          uint32_t sfa_t = 0, sfb_t = 0;
-          if constexpr (kFP4) {
-            copy_scales(stage);
-            sfa_t = tmem_base + uint32_t(Cfg::SF_TMEM_BASE + stage * Cfg::SF_COLS);
-            sfb_t = sfa_t + Cfg::KSTEPS * 4;
-          }
+          // the next job, filled in between this job's MMAs
+          int n_tile = tile, n_kb = kb + 1, n_kb_begin = kb_begin, n_kb_end = kb_end;
+          int n_it = it, n_acc = acc;
+          bool has_next = true, next_ready = true;
           // (the full barrier orders the TMA data before these MMAs; no
           // tcgen05 fence is needed per stage)
 #pragma unroll
           for (int j = 0; j < Cfg::KSTEPS; ++j) {
+            copy_scales_for(sfa_t, soff, j);
             if (j < nsteps) {
               // step j: K sub-tile j / 4, 32-byte K slice j % 4 within it
               const uint64_t ad =
                   adesc0 + soff + uint64_t(((j / 4) * Cfg::A_SUB_BYTES + 32 * (j % 4)) >> 4);
               const uint64_t bd =
                   bdesc0 + soff + uint64_t(((j / 4) * Cfg::B_SUB_BYTES + 32 * (j % 4)) >> 4);
-              const uint32_t accum = (kb != kb_begin) || (j != 0);
+              const uint32_t accum = !first_kb || (j != 0);
               if constexpr (kFP4)
                 ptx::mma_nvf4<CG>(d_tmem, ad, bd, idesc, sfa_t + 4 * j,
-                                  sfb_t + j * 4 * Cfg::SFB_ATOMS, accum);
+                                  sfa_t + Cfg::KSTEPS * 4 + j * 4 * Cfg::SFB_ATOMS, accum);
               else
                 ptx::mma_bf16<CG>(d_tmem, ad, bd, idesc, accum);
             }
             if (j == 0 && pending_empty >= 0)
               ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
-            if (j == (Cfg::KSTEPS > 2 ? 1 : 0) && has_next)
-              next_ready = ptx::mbar_test_wait(full_bar(nstage), nphase);
+            if (j == kPrep) {
+              if (last_kb) {
+                n_tile = tile + num_clusters;
+                has_next = n_tile < p.total_tiles;
+                if (has_next) {
+                  int l2, mb2, nb2;
+                  decode_tile<Cfg>(n_tile, p, pair, l2, mb2, nb2);
+                  n_kb_begin = (p.k_splits > 1) ? l2 * p.kb_per_split : 0;
+                  n_kb_end = min(p.num_k_blocks, n_kb_begin + p.kb_per_split);
+                  n_kb = n_kb_begin;
+                  n_it = it + 1;
+                  n_acc = n_it % Cfg::NUM_ACC;
+                  if constexpr (Cfg::NUM_ACC == 2) {
+                    // the other accumulator: its previous tile's epilogue
+                    // must have read it (independent of this tile's MMAs)
+                    ok = wait_bar(acc_empty(n_acc), (uint32_t(n_it / 2) & 1u) ^ 1u, w, 2);
+                    ptx::tc_fence_after();
+                  }
+                }
+              }
+              if (has_next) next_ready = ptx::mbar_test_wait(full_bar(nstage), nphase);
+            }
           }
           if (last_kb) {
             // tile done: release the stage and hand the accumulator over now
@@ -557,29 +578,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           } else {
             pending_empty = stage;
           }
-          if (!has_next) break;
-          stage = nstage;
-          phase = nphase;
-          if (last_kb) {
-            tile = next_tile;
-            ++it;
-            decode_tile<Cfg>(tile, p, pair, l, mb, nb);
-            kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
-            kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
-            kb = kb_begin;
-            acc = it % Cfg::NUM_ACC;
-            if (!wait_bar(acc_empty(acc), (uint32_t(it / Cfg::NUM_ACC) & 1u) ^ 1u, w, 2)) {
-              ok = false;
-              break;
+          if (!has_next || !ok) break;
+          if constexpr (Cfg::NUM_ACC == 1) {
+            // a single accumulator: the epilogue of the tile just committed
+            // must have read it before the next tile's first MMA
+            if (last_kb) {
+              if (!wait_bar(acc_empty(n_acc), (uint32_t(n_it) & 1u) ^ 1u, w, 2)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
             }
-            ptx::tc_fence_after();
-          } else {
-            ++kb;
           }
-          if (!next_ready && !wait_bar(full_bar(stage), phase, w, 3)) {
+          if (!next_ready && !wait_bar(full_bar(nstage), nphase, w, 3)) {
             ok = false;
             break;
           }
+          stage = nstage;
+          phase = nphase;
+          tile = n_tile;
+          kb = n_kb;
+          kb_begin = n_kb_begin;
+          kb_end = n_kb_end;
+          it = n_it;
+          acc = n_acc;
         }
         if (pending_empty >= 0) ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
       }
