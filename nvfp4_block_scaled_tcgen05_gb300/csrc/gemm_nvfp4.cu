@@ -5,25 +5,32 @@
 //
 // Each 256-element K stage carries, per 128 rows, the 4 consecutive 512-byte
 // scale atoms of that K range (2 KB, contiguous in the hardware layout),
-// which tcgen05.cp moves into a per-stage TMEM slot ahead of the stage's 4
-// MMAs.  The MMA reads the scales of row 32*i + g from TMEM lane 32*i + g;
-// staging every atom four times in shared memory (one TMA box whose replica
-// dimension has stride 0) lets one 128-lane x 32-byte copy fill the scale
-// columns of two A atoms or of one MMA's two B atoms: 6 copies per stage
-// instead of 12, which the tensor pipe needs (measured 256 -> 201 us at
-// 4096 x 7168 x 16384).  One TMEM accumulator (256 columns) plus the scale
-// slots fill the 512 columns, so the epilogue is register-staged: 8 warps
-// read the whole accumulator, release it, then convert and store straight
-// to global memory while the next tile's MMAs run.
+// which tcgen05.cp moves into a per-stage TMEM slot before the stage's 4
+// MMAs.  The MMA reads the scales of row 32*i + g from TMEM lane 32*i + g,
+// column base + i, so an atom has to land in all four 32-lane quarters:
+//   * A scales are staged four times in shared memory (one TMA box whose
+//     replica dimension has stride 0), so one 128-lane x 32-byte copy fills
+//     the scale columns of two MMAs (2 copies per stage);
+//   * B scales (the two atoms of a 256-row B tile) are staged once and
+//     copied with the replicating 32x128b.warpx4 shape (8 copies per stage),
+//     which reads 4x fewer shared-memory bytes than staging them replicated.
+// A dedicated warp issues the copies and signals the MMA thread through a
+// per-stage barrier, so the MMA thread issues only MMAs.  Measured at
+// 4096 x 7168 x 16384 on GB300: 228 us with both scale sets replicated and
+// copied by the MMA thread, 191 us with this arrangement and 5 stages.
+// One TMEM accumulator (256 columns) plus the scale slots fill the 512
+// columns, so the epilogue is register-staged: 8 warps read the whole
+// accumulator, release it, then convert and store straight to global
+// memory while the next tile's MMAs run.
 //
 // Configurations: pair (cta_group::2, 256 x 256 tiles, each CTA stages its
-// 128 A rows, 128 B rows and the scales of all 256 B rows, 4 stages) and
+// 128 A rows, 128 B rows and the scales of all 256 B rows, 5 stages) and
 // single (cta_group::1, 128 x 256 tiles, 3 stages) for small problems.
 #include "launch.cuh"
 
 namespace gb300 {
 
-using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 4, 8, 0, true, true>;
+using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 0, true, false>;
 using Nvfp4Single = TileCfg<Operand::kNVFP4, 1, 256, 3, 8, 1>;
 
 template <class Cfg>

@@ -124,12 +124,18 @@ struct TileCfg {
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
   static_assert(EPI_COLS % 64 == 0, "epilogue columns per warp");
   static_assert(NUM_ACC == 2 || kRegEpi, "a single accumulator needs the register-staged epilogue");
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], epi[W][B], mma_done
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1;
+  // NVFP4: dedicated warps move each stage's scale atoms into TMEM and
+  // signal sf_full[stage]; the MMA thread then issues only MMAs (every
+  // tcgen05 instruction costs the issuing thread tens of cycles).  With
+  // SF_WARPS = 2 the two warps take alternate stages.
+  static constexpr int SF_WARPS = kFP4 ? 2 : 0;
+  static constexpr bool SF_WARP = SF_WARPS > 0;
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], epi[W][B], mma_done, sf_full[S]
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1 + (SF_WARP ? STAGES : 0);
   static constexpr int BAR_BYTES = NUM_BARS * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * SF_WARPS;
   static constexpr int GROUP_M = 8;
 
   // Instruction descriptor.  kind::f16: D=F32 (bits 4-5 = 1), A=B=BF16
@@ -261,6 +267,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     return bar_base + 8 * (2 * STAGES + 4 + e * Cfg::EPI_BUFS + b);
   };
   const uint32_t mma_done = bar_base + 8 * (2 * STAGES + 4 + Cfg::EPI_WARPS * Cfg::EPI_BUFS);
+  auto sf_full = [&](int s) { return mma_done + 8 * (1 + s); };
+  // the barrier that says stage s may be multiplied: its TMA data landed,
+  // and (NVFP4) its scales are in TMEM
+  auto ready_bar = [&](int s) { return Cfg::SF_WARP ? sf_full(s) : full_bar(s); };
   uint8_t* misc = smem + (bar_base - sbase) + 8 * Cfg::NUM_BARS;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + 4);
@@ -292,6 +302,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     for (int e = 0; e < Cfg::EPI_WARPS; ++e)
       for (int b = 0; b < Cfg::EPI_BUFS; ++b) ptx::mbar_init(epi_bar(e, b), 1);
     ptx::mbar_init(mma_done, 1);
+    if constexpr (Cfg::SF_WARP)
+      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(sf_full(s), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -313,6 +325,45 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Watch w{abort_flag, p.status, p.timeout_ns};
+
+  // NVFP4: the scale atoms of MMA j of stage s go into the stage's TMEM
+  // slot (issued by the scale warp, which then commits sf_full[s]).
+  // Descriptors and TMEM addresses of stage 0; stage s adds
+  // s * STAGE_BYTES >> 4 to a descriptor's start field (no carry, as
+  // for the operand descriptors) and s * SF_COLS to a TMEM column.
+  const uint32_t sf_t0 = tmem_base + uint32_t(Cfg::SF_TMEM_BASE);
+  uint64_t sfa_d0 = 0, sfb_d0 = 0;
+  if constexpr (kFP4) {
+    sfa_d0 = Cfg::SFA_REP ? ptx::smem_desc(stage_sfa(0), 4 * Cfg::SF_ATOM, 128, 0)
+                          : ptx::smem_desc(stage_sfa(0), 0, 128, 0);
+    sfb_d0 = Cfg::SFB_REP ? ptx::smem_desc(stage_sfb(0), Cfg::SFB_ATOM_BYTES, 128, 0)
+                          : ptx::smem_desc(stage_sfb(0), 0, 128, 0);
+  }
+  auto copy_scales_for = [&](uint32_t sfa_t, uint64_t soff, int j) {
+    if constexpr (kFP4) {
+      const uint32_t sfb_t = sfa_t + Cfg::KSTEPS * 4;
+      if constexpr (Cfg::SFA_REP) {
+        // replicas of atoms j and j+1 -> lanes 0..127, columns 4j .. 4j+7
+        if (j % 2 == 0)
+          ptx::tc_cp_128x256b<CG>(sfa_t + 4 * j,
+                                  sfa_d0 + soff + uint64_t((4 * j * Cfg::SF_ATOM) >> 4));
+      } else {
+        ptx::tc_cp_32x128b_warpx4<CG>(sfa_t + 4 * j,
+                                      sfa_d0 + soff + uint64_t((j * Cfg::SF_ATOM) >> 4));
+      }
+      if constexpr (Cfg::SFB_REP) {
+        // replicas of B atom 0 (columns +0..3) and atom 1 (+4..7)
+        ptx::tc_cp_128x256b<CG>(sfb_t + 8 * j,
+                                sfb_d0 + soff + uint64_t((4 * j * Cfg::SF_ATOM) >> 4));
+      } else {
+#pragma unroll
+        for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
+          ptx::tc_cp_32x128b_warpx4<CG>(
+              sfb_t + j * 4 * Cfg::SFB_ATOMS + 4 * at,
+              sfb_d0 + soff + uint64_t(((at * Cfg::KSTEPS + j) * Cfg::SF_ATOM) >> 4));
+      }
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -439,47 +490,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = Cfg::idesc();
-      // NVFP4: the scale atoms of MMA j of stage s go into the stage's TMEM
-      // slot right before that MMA (tcgen05.cp and tcgen05.mma from one
-      // thread execute in order).  Spread between the MMAs the copies
-      // overlap MMA execution; bunched in front of a stage's MMAs they held
-      // the tensor pipe near 70% of its FP4 rate on GB300 (90% interleaved).
-      // Descriptors and TMEM addresses of stage 0; stage s adds
-      // s * STAGE_BYTES >> 4 to a descriptor's start field (no carry, as
-      // for the operand descriptors) and s * SF_COLS to a TMEM column.
-      const uint32_t sf_t0 = tmem_base + uint32_t(Cfg::SF_TMEM_BASE);
-      uint64_t sfa_d0 = 0, sfb_d0 = 0;
-      if constexpr (kFP4) {
-        sfa_d0 = Cfg::SFA_REP ? ptx::smem_desc(stage_sfa(0), 4 * Cfg::SF_ATOM, 128, 0)
-                              : ptx::smem_desc(stage_sfa(0), 0, 128, 0);
-        sfb_d0 = Cfg::SFB_REP ? ptx::smem_desc(stage_sfb(0), Cfg::SFB_ATOM_BYTES, 128, 0)
-                              : ptx::smem_desc(stage_sfb(0), 0, 128, 0);
-      }
-      auto copy_scales_for = [&](uint32_t sfa_t, uint64_t soff, int j) {
-        if constexpr (kFP4) {
-          const uint32_t sfb_t = sfa_t + Cfg::KSTEPS * 4;
-          if constexpr (Cfg::SFA_REP) {
-            // replicas of atoms j and j+1 -> lanes 0..127, columns 4j .. 4j+7
-            if (j % 2 == 0)
-              ptx::tc_cp_128x256b<CG>(sfa_t + 4 * j,
-                                      sfa_d0 + soff + uint64_t((4 * j * Cfg::SF_ATOM) >> 4));
-          } else {
-            ptx::tc_cp_32x128b_warpx4<CG>(sfa_t + 4 * j,
-                                          sfa_d0 + soff + uint64_t((j * Cfg::SF_ATOM) >> 4));
-          }
-          if constexpr (Cfg::SFB_REP) {
-            // replicas of B atom 0 (columns +0..3) and atom 1 (+4..7)
-            ptx::tc_cp_128x256b<CG>(sfb_t + 8 * j,
-                                    sfb_d0 + soff + uint64_t((4 * j * Cfg::SF_ATOM) >> 4));
-          } else {
-#pragma unroll
-            for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
-              ptx::tc_cp_32x128b_warpx4<CG>(
-                  sfb_t + j * 4 * Cfg::SFB_ATOMS + 4 * at,
-                  sfb_d0 + soff + uint64_t(((at * Cfg::KSTEPS + j) * Cfg::SF_ATOM) >> 4));
-          }
-        }
-      };
       // The tensor pipe holds little more than the MMA it is executing, so
       // thread work between a stage's last MMA and the next stage's first
       // MMA leaves it idle, and every tcgen05 instruction costs the issuing
@@ -507,7 +517,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
         int kb = kb_begin;
         int it = 0, acc = 0;
-        ok = wait_bar(acc_empty(0), 1u, w, 2) && wait_bar(full_bar(0), 0u, w, 3);
+        ok = wait_bar(acc_empty(0), 1u, w, 2) && wait_bar(ready_bar(0), 0u, w, 3);
         ptx::tc_fence_after();
         // Stage s, MMA j: start address + s * STAGE_BYTES + offset of j, i.e.
         // the 14-bit start field (address >> 4) grows by that >> 4; shared
@@ -531,7 +541,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           // tcgen05 fence is needed per stage)
 #pragma unroll
           for (int j = 0; j < Cfg::KSTEPS; ++j) {
-            copy_scales_for(sfa_t, soff, j);
+            if constexpr (!Cfg::SF_WARP) copy_scales_for(sfa_t, soff, j);
             if (j < nsteps) {
               // step j: K sub-tile j / 4, 32-byte K slice j % 4 within it
               const uint64_t ad =
@@ -567,7 +577,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                   }
                 }
               }
-              if (has_next) next_ready = ptx::mbar_test_wait(full_bar(nstage), nphase);
+              if (has_next) next_ready = ptx::mbar_test_wait(ready_bar(nstage), nphase);
             }
           }
           if (last_kb) {
@@ -590,10 +600,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               ptx::tc_fence_after();
             }
           }
-          if (!next_ready && !wait_bar(full_bar(nstage), nphase, w, 3)) {
+          if (!next_ready && !wait_bar(ready_bar(nstage), nphase, w, 3)) {
             ok = false;
             break;
           }
+          // scales written by another thread: order them before the MMAs
+          if constexpr (Cfg::SF_WARP) ptx::tc_fence_after();
           stage = nstage;
           phase = nphase;
           tile = n_tile;
@@ -608,6 +620,48 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // Every MMA / copy issued must be complete before TMEM is released.
       ptx::tc_commit<CG>(mma_done, pair_mask);
       drain_bar(mma_done, 0, w);
+    }
+  } else if (Cfg::SF_WARP && warp >= 2 + Cfg::EPI_WARPS) {
+    // ------------------------------------------------------------ scale copies
+    // Walks the same stage sequence as the MMA issuer: once a stage's TMA
+    // data has landed (which also means the MMAs that last read the
+    // stage's TMEM scale slot are done: the producer refilled the stage
+    // only after their release), copy its scale atoms and commit sf_full.
+    const int sfw = warp - (2 + Cfg::EPI_WARPS);  // this warp takes jobs sfw, sfw + SF_WARPS, ...
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int last = -1;
+      uint32_t last_phase = 0;
+      bool ok = true;
+      int job = 0;
+      for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters) {
+        int l, mb, nb;
+        decode_tile<Cfg>(tile, p, pair, l, mb, nb);
+        const int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
+        const int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
+          if (job % Cfg::SF_WARPS == sfw) {
+            if (!wait_bar(full_bar(stage), phase, w, 6)) {
+              ok = false;
+              break;
+            }
+            const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
+            const uint32_t sfa_t = sf_t0 + uint32_t(stage * Cfg::SF_COLS);
+#pragma unroll
+            for (int j = 0; j < Cfg::KSTEPS; ++j) copy_scales_for(sfa_t, soff, j);
+            ptx::tc_commit<CG>(sf_full(stage), uint16_t(1u << pair_leader));
+            last = stage;
+            last_phase = phase;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy must be complete before TMEM is released
+      if (last >= 0) drain_bar(sf_full(last), last_phase, w);
     }
   } else {
     // ------------------------------------------------------------ epilogue
