@@ -128,6 +128,10 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   if (scaled_acc && K <= kStreamMaxK)
     return cg == 2 ? run_bf16<Bf16PairStream>(A, B, C, M, N, K, scale, true, dev, stream)
                    : run_bf16<Bf16SingleStream>(A, B, C, M, N, K, scale, true, dev, stream);
+  // Plain outputs: a CTA pair covers 256 rows with the same per-SM work as
+  // one CTA on 128 rows, so pairs (128-deep stages, half the B traffic per
+  // SM) occupy as many SMs as single CTAs whenever M spans two row blocks.
+  if (!scaled_acc && !cta_group_override()) cg = (M > 128) ? 2 : 1;
   if (!scaled_acc && cg == 2) {
     // GB300GEMM_MC=2 selects the A-multicast cluster; measured no faster
     // than the plain pair on the shapes here (GB300), so it is opt-in.
