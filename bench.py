@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-warm-s", type=float, default=0.6,
                     help="extra warm-up seconds so that clock samples cover the load")
-    ap.add_argument("--shapes", default="down,qkv,gqa,gqa_splitk,lora,router,nvfp4",
+    ap.add_argument("--shapes", default="down,qkv,gqa,gqa_splitk,lora,router,nvfp4,nvfp4_decode",
                     help="comma list of the extra shapes to measure")
     ap.add_argument("--no-headline", action="store_true",
                     help="profiling aid: measure only --shapes and print them")
@@ -433,6 +433,10 @@ def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
         out.append(measure_router(torch, lib, synth, up, stream, dev, warmup, reps, check))
     if "nvfp4" in which:
         out.append(measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_peak))
+    if "nvfp4_decode" in which:
+        for name in sorted(synth.NVFP4_DECODE):
+            out.append(measure_nvfp4_decode(torch, lib, synth, up, stream, dev, pk, warmup, reps,
+                                            check, fp4_peak, name))
     assert lib.gemm_get_device_status(sp) == 0
     return out
 
@@ -538,6 +542,36 @@ def measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_p
            # tensor pipe's own ceiling is 4x the bf16 peak
            "frac_fp4_mma_rate": tf / (fp4_peak * 4.0 / FP4_PEAK_RATIO)}
     del sets, cs
+    return res
+
+
+def measure_nvfp4_decode(torch, lib, synth, up, stream, dev, pk, warmup, reps, check, fp4_peak,
+                         name):
+    """NVFP4 at decode-like M = 128 with split-K (FP32 partials + ordered reduce).
+    Weight-bandwidth bound: reported against HBM as well as the FP4 peak."""
+    sp = stream.cuda_stream
+    w, k_splits = synth.NVFP4_DECODE[name]
+    a_h, b_h, sfa_h, sfb_h = synth.nvfp4_inputs(w)
+    ws_bytes = lib.gemm_nvfp4_bs_splitk_workspace_bytes(w.M, w.N, w.K, k_splits)
+    set_bytes = a_h.size + b_h.size + sfa_h.size + sfb_h.size + w.M * w.N * 2
+    n = n_sets_for(set_bytes)
+    a0, b0, sa0, sb0 = up(a_h), up(b_h), up(sfa_h), up(sfb_h)
+    sets = [(a0, b0, sa0, sb0)] + [(a0.clone(), b0.clone(), sa0.clone(), sb0.clone())
+                                   for _ in range(n - 1)]
+    cs = [torch.empty((1, w.M, w.N), dtype=torch.float16, device=dev) for _ in range(n)]
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    fn = lambda i: check(lib.gemm_nvfp4_bs_splitk(
+        sets[i][0].data_ptr(), sets[i][1].data_ptr(), sets[i][2].data_ptr(), sets[i][3].data_ptr(),
+        cs[i].data_ptr(), ws.data_ptr(), ws_bytes, 1, w.M, w.N, w.K, k_splits, sp))
+    sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+    gbs = set_bytes / sec / 1e9
+    res = {"shape": name, "L": 1, "M": w.M, "N": w.N, "K": w.K, "k_splits": k_splits,
+           "us": sec * 1e6, "TFLOP/s": tf, "frac_fp4_peak": tf / fp4_peak,
+           "GB/s": gbs, "frac_hbm_peak": gbs / pk["hbm_gbs"],
+           "bytes": int(set_bytes), "note": "operands + scales + fp16 output; split-K workspace "
+           "traffic (L2-resident) not counted"}
+    del sets, cs, ws
     return res
 
 

@@ -1,7 +1,8 @@
 // bf16_scaled_add: out[i] = bf16(float(out[i]) + scale * float(d[i])), the
 // second kernel of the unfused LoRA pair ("gemm_dense.rs",
-// dense_gemm_tc_scaled_acc doc comment).  HBM-bound streaming kernel: 16-byte
-// vector loads/stores, grid sized to a multiple of the SM count.
+// dense_gemm_tc_scaled_acc doc comment), and the ordered split-K reduce.
+// HBM-bound streaming kernels: 16-byte vector loads/stores, grid sized to a
+// multiple of the SM count.
 #include <algorithm>
 
 #include "epilogue_math.cuh"
@@ -36,8 +37,16 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// C[i] = bf16(ws[0][i] + ws[1][i] + ... + ws[S-1][i]), FP32 adds in split
-// order (deterministic); 8 outputs per thread, 16-byte accesses.
+// C[i] = out16(ws[0][i] + ws[1][i] + ... + ws[S-1][i]), FP32 adds in split
+// order (deterministic), then one RNE to BF16 or FP16; 8 outputs per thread,
+// 16-byte accesses.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_out16(uint32_t lo, uint32_t hi) {
+  if constexpr (kF16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, uint16_t* __restrict__ C, size_t n,
                          int splits) {
@@ -55,10 +64,10 @@ __global__ void __launch_bounds__(kThreads)
       b.z = __fadd_rn(b.z, y.z); b.w = __fadd_rn(b.w, y.w);
     }
     uint4 o;
-    o.x = pack_bf16x2(__float_as_uint(a.x), __float_as_uint(a.y));
-    o.y = pack_bf16x2(__float_as_uint(a.z), __float_as_uint(a.w));
-    o.z = pack_bf16x2(__float_as_uint(b.x), __float_as_uint(b.y));
-    o.w = pack_bf16x2(__float_as_uint(b.z), __float_as_uint(b.w));
+    o.x = pack_out16<kF16>(__float_as_uint(a.x), __float_as_uint(a.y));
+    o.y = pack_out16<kF16>(__float_as_uint(a.z), __float_as_uint(a.w));
+    o.z = pack_out16<kF16>(__float_as_uint(b.x), __float_as_uint(b.y));
+    o.w = pack_out16<kF16>(__float_as_uint(b.z), __float_as_uint(b.w));
     reinterpret_cast<uint4*>(C)[i] = o;
   }
   const size_t tail = n - nvec * 8;
@@ -66,7 +75,7 @@ __global__ void __launch_bounds__(kThreads)
     const size_t idx = nvec * 8 + threadIdx.x;
     float a = ws[idx];
     for (int s = 1; s < splits; ++s) a = __fadd_rn(a, ws[size_t(s) * n + idx]);
-    C[idx] = uint16_t(pack_bf16x2(__float_as_uint(a), 0u) & 0xFFFFu);
+    C[idx] = uint16_t(pack_out16<kF16>(__float_as_uint(a), 0u) & 0xFFFFu);
   }
 }
 
@@ -77,7 +86,18 @@ int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const D
   const size_t nvec = n / 8;
   const size_t want = (nvec + kThreads - 1) / kThreads;
   const int grid = int(std::max<size_t>(1, std::min<size_t>(want, size_t(dev.num_sms) * 8)));
-  splitk_reduce_kernel<<<grid, kThreads, 0, stream>>>(ws, static_cast<uint16_t*>(C), n, splits);
+  splitk_reduce_kernel<false><<<grid, kThreads, 0, stream>>>(ws, static_cast<uint16_t*>(C), n,
+                                                             splits);
+  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+int launch_splitk_reduce_f16(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
+                             cudaStream_t stream) {
+  const size_t nvec = n / 8;
+  const size_t want = (nvec + kThreads - 1) / kThreads;
+  const int grid = int(std::max<size_t>(1, std::min<size_t>(want, size_t(dev.num_sms) * 8)));
+  splitk_reduce_kernel<true><<<grid, kThreads, 0, stream>>>(ws, static_cast<uint16_t*>(C), n,
+                                                            splits);
   return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 

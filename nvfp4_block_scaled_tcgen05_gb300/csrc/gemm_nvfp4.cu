@@ -23,19 +23,30 @@
 // accumulator, release it, then convert and store straight to global
 // memory while the next tile's MMAs run.
 //
-// Configurations: pair (cta_group::2, 256 x 256 tiles, each CTA stages its
-// 128 A rows, 128 B rows and the scales of all 256 B rows, 5 stages) and
-// single (cta_group::1, 128 x 256 tiles, 3 stages) for small problems.
+// Configuration: CTA pairs (cta_group::2, 256 x 256 tiles, each CTA stages
+// its 128 A rows, 128 B rows and the scales of all 256 B rows, 5 stages)
+// for every shape; with M = 128 the second CTA's rows lie past M (its loads
+// are zero-filled, its stores skipped).  A single-CTA configuration
+// (cta_group::1, 128 x 256 tiles, 3 stages, scale-copy warps) faulted the
+// GPU twice when launched back to back; the cause was not found, so it is
+// not used.
+// Split-K (decode-like M = 128 with few output tiles): the pair
+// configuration writes FP32 partials of K-block chunks straight from
+// registers into a caller workspace, then an ordered reduce rounds once to
+// FP16 ("gemm_dense.rs", dense_gemm_splitk, applied to the block-scaled GEMM).
 #include "launch.cuh"
 
 namespace gb300 {
 
 using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 0, true, false>;
-using Nvfp4Single = TileCfg<Operand::kNVFP4, 1, 256, 3, 8, 1>;
 
-template <class Cfg>
-static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
-                     int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+// `out` is the FP16 output (EPI = kStoreFP16) or, with splits > 1 (L = 1),
+// the FP32 workspace [splits][M][N] (EPI = kStoreF32).
+template <class Cfg, Epilogue EPI = Epilogue::kStoreFP16>
+static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* out,
+                     int L, int M, int N, int K, int splits, int kb_per_split,
+                     const DeviceInfo& dev, cudaStream_t stream) {
+  void* c = out;
   CUtensorMap ta, tb, tc, tsa, tsb;
   const uint64_t kb = uint64_t(K) / 2;  // bytes per packed row
   const int rest_m = M / 128, rest_n = N / 128, rest_k = K / 64;
@@ -72,29 +83,44 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
   p.M = M;
   p.N = N;
   p.K = K;
-  p.L = L;
+  p.L = splits > 1 ? splits : L;  // with split-K the batch slot indexes the split
   p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = K / Cfg::BK;
-  p.total_tiles = p.num_m_blocks * p.num_n_blocks * L;
-  p.k_splits = 1;
-  p.kb_per_split = p.num_k_blocks;
+  p.total_tiles = p.num_m_blocks * p.num_n_blocks * p.L;
+  p.k_splits = splits;
+  p.kb_per_split = splits > 1 ? kb_per_split : p.num_k_blocks;
   p.rest_m = rest_m;
   p.rest_n = rest_n;
   p.rest_k = rest_k;
   p.c_ptr = c;
   p.status = dev.status;
   p.timeout_ns = wait_timeout_ns();
-  return launch_tcgen05<Cfg, Epilogue::kStoreFP16>(ta, tb, tc, tsa, tsb, p, dev, stream);
+  return launch_tcgen05<Cfg, EPI>(ta, tb, tc, tsa, tsb, p, dev, stream);
 }
 
 int launch_gemm_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
                       int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  const long long pair_tiles = (long long)L * ((M + 255) / 256) * ((N + 255) / 256);
-  int cg = (pair_tiles >= dev.num_sms / 2) ? 2 : 1;
-  if (const int o = cta_group_override()) cg = o;
-  return cg == 2 ? run_nvfp4<Nvfp4Pair>(a, b, sfa, sfb, c, L, M, N, K, dev, stream)
-                 : run_nvfp4<Nvfp4Single>(a, b, sfa, sfb, c, L, M, N, K, dev, stream);
+  return run_nvfp4<Nvfp4Pair>(a, b, sfa, sfb, c, L, M, N, K, 1, 0, dev, stream);
+}
+
+int nvfp4_splitk_effective_splits(int K, int splits, int* kb_per_split) {
+  const int nkb = K / Nvfp4Pair::BK;
+  if (splits > nkb) splits = nkb;
+  const int kbps = (nkb + splits - 1) / splits;
+  *kb_per_split = kbps;
+  return (nkb + kbps - 1) / kbps;  // every split non-empty
+}
+
+int launch_gemm_nvfp4_splitk(const void* a, const void* b, const void* sfa, const void* sfb,
+                             void* c, float* ws, int M, int N, int K, int splits,
+                             const DeviceInfo& dev, cudaStream_t stream) {
+  int kbps = 0;
+  const int s_eff = nvfp4_splitk_effective_splits(K, splits, &kbps);
+  const int rc = run_nvfp4<Nvfp4Pair, Epilogue::kStoreF32>(a, b, sfa, sfb, ws, 1, M, N, K, s_eff,
+                                                            kbps, dev, stream);
+  if (rc != GEMM_OK) return rc;
+  return launch_splitk_reduce_f16(ws, c, size_t(M) * N, s_eff, dev, stream);
 }
 
 }  // namespace gb300

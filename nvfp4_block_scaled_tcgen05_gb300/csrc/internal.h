@@ -56,8 +56,17 @@ int launch_selftest_timeout(int timeout_ms, const DeviceInfo& dev, cudaStream_t 
 int splitk_effective_splits(int K, int splits, int* kb_per_split);
 int launch_gemm_bf16_splitk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
                             int splits, const DeviceInfo& dev, cudaStream_t stream);
-// C[i] = bf16(sum_{s=0..S-1} ws[s*n + i]) in split order.
+// NVFP4 split-K (L == 1): S = min(k_splits, K/256) chunks of whole 256-deep
+// K blocks, reduced so every chunk is non-empty; FP32 partials in
+// ws[S][M][N], then an ordered reduce to FP16.
+int nvfp4_splitk_effective_splits(int K, int splits, int* kb_per_split);
+int launch_gemm_nvfp4_splitk(const void* a, const void* b, const void* sfa, const void* sfb,
+                             void* c, float* ws, int M, int N, int K, int splits,
+                             const DeviceInfo& dev, cudaStream_t stream);
+// C[i] = bf16(sum_{s=0..S-1} ws[s*n + i]) in split order (_f16: FP16).
 int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
                          cudaStream_t stream);
+int launch_splitk_reduce_f16(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
+                             cudaStream_t stream);
 
 }  // namespace gb300

@@ -243,8 +243,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // Without epilogue buffers the 16-bit outputs are written straight from
   // registers with 16-byte global stores (frees shared memory for stages).
   constexpr bool kDirectStore = (Cfg::EPI_BUFS == 0);
-  static_assert(!kDirectStore || EPI == Epilogue::kStoreBF16 || EPI == Epilogue::kStoreFP16,
-                "direct stores serve the plain 16-bit epilogues");
+  static_assert(!kDirectStore || EPI == Epilogue::kStoreBF16 || EPI == Epilogue::kStoreFP16 ||
+                    (EPI == Epilogue::kStoreF32 && Cfg::kRegEpi),
+                "direct stores serve the plain 16-bit epilogues and register-staged FP32 partials");
   // L2 policy hints: keep the operands resident (they are re-read by other
   // tiles), let the once-written output leave first.
   constexpr bool kHintLoads = true;
@@ -646,6 +647,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               ok = false;
               break;
             }
+            // The slot's previous readers (MMAs of the MMA thread) completed
+            // before this stage could be refilled; order this thread's
+            // copies after that observed completion.
+            ptx::tc_fence_after();
             const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
             const uint32_t sfa_t = sf_t0 + uint32_t(stage * Cfg::SF_COLS);
 #pragma unroll
@@ -748,7 +753,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 2 * NCH; ++i) ptx::tmem_ld_wait_regs(r[i]);
         release_acc(acc);
-        if constexpr (kDirectStore) {
+        if constexpr (kDirectStore && EPI == Epilogue::kStoreF32) {
+          // FP32 split-K partials: 32 columns per TMEM read, eight 16-byte
+          // stores per lane (N % 4 == 0 keeps every piece whole)
+          const int grow = row0 + lane;
+          if (grow < p.M) {
+            float* dst = static_cast<float*>(p.c_ptr) +
+                         (size_t(l) * p.M + size_t(grow)) * size_t(p.N) + nb * BN + col_base;
+#pragma unroll
+            for (int i = 0; i < 2 * NCH; ++i)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (nb * BN + col_base + 32 * i + 4 * j < p.N)
+                  *reinterpret_cast<uint4*>(dst + 32 * i + 4 * j) =
+                      make_uint4(r[i][4 * j], r[i][4 * j + 1], r[i][4 * j + 2], r[i][4 * j + 3]);
+          }
+        } else if constexpr (kDirectStore) {
           const int grow = row0 + lane;
           if (grow < p.M) {
             uint16_t* dst = static_cast<uint16_t*>(p.c_ptr) +

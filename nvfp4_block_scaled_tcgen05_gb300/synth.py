@@ -105,6 +105,13 @@ class Nvfp4:
 
 
 NVFP4 = Nvfp4("nvfp4", 1, 4096, 7168, 16384, 1004)
+# decode-like shapes of the NVFP4 page's benchmark (M = 128), run with
+# split-K; the split count fills the SMs with (N/256) x splits CTA pairs
+# (at most 76 pairs on 152 SMs)
+NVFP4_DECODE = {
+    "nvfp4_decode_7168x16384": (Nvfp4("nvfp4_decode_7168x16384", 1, 128, 7168, 16384, 1005), 2),
+    "nvfp4_decode_4096x7168": (Nvfp4("nvfp4_decode_4096x7168", 1, 128, 4096, 7168, 1006), 4),
+}
 
 
 def gemm_inputs(w: Gemm, seed_offset: int = 0):

@@ -136,3 +136,29 @@ def test_splitk_rejects_bad_arguments(lib):
     assert f(P, 2 * P, 3 * P, 4 * P, 16, 64, 64, 256, 2, None) == 2    # workspace too small
     assert f(P, 2 * P, 3 * P, 4 * P + 8, big, 8, 8, 64, 2, None) == 3  # misaligned workspace
     assert f(P, 2 * P, 3 * P, P + 16, big, 8, 8, 64, 2, None) == 4     # workspace overlaps A
+
+
+def test_nvfp4_splitk_workspace_size_rules(lib):
+    ws = lib.gemm_nvfp4_bs_splitk_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(128, 7168, 16384, 5) == 5 * 128 * 7168 * 4      # 64 blocks: 13 per split, 5 splits
+    assert ws(128, 4096, 7168, 7) == 7 * 128 * 4096 * 4       # 28 blocks: 4 per split
+    assert ws(128, 256, 1024, 3) == 2 * 128 * 256 * 4         # 4 blocks: 2 per split, 2 splits
+    assert ws(128, 256, 512, 64) == 2 * 128 * 256 * 4         # capped at K/256 = 2
+    assert ws(128, 256, 1000, 2) == 0 and ws(128, 256, 1024, 0) == 0 and ws(0, 256, 1024, 2) == 0
+
+
+def test_nvfp4_splitk_rejects_bad_arguments(lib):
+    f = lib.gemm_nvfp4_bs_splitk
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_size_t] + [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    big = 1 << 30
+    ok = (P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P, big)
+    assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 0, big, 1, 128, 256, 1024, 2, None) == 1  # NULL ws
+    assert f(*ok, 2, 128, 256, 1024, 2, None) == 2            # L != 1
+    assert f(*ok, 1, 100, 256, 1024, 2, None) == 2            # M % 128
+    assert f(*ok, 1, 128, 256, 1000, 2, None) == 2            # K % 256
+    assert f(*ok, 1, 128, 256, 1024, 0, None) == 2            # k_splits < 1
+    assert f(*ok, 1, 128, 256, 1024, 65, None) == 2           # k_splits > 64
+    assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P, 16, 1, 128, 256, 1024, 2, None) == 2  # small ws
+    assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P + 8, big, 1, 128, 256, 1024, 2, None) == 3
+    assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, P + 16, big, 1, 128, 256, 1024, 2, None) == 4  # ws on a

@@ -29,10 +29,10 @@ def g():
     assert lib.gemm_get_device_status() == 0
 
 
-@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
-def cg(request, monkeypatch):
-    """Force the single-CTA or the CTA-pair (cta_group::2) kernel."""
-    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(request.param))
+@pytest.fixture(params=[2], ids=["cta2"])
+def cg(request):
+    """The NVFP4 GEMM always runs on CTA pairs (cta_group::2); M = 128
+    problems leave the second CTA's rows past M."""
     return request.param
 
 
@@ -112,3 +112,52 @@ def test_full_size_sampled(g):
     ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, w.L, w.M, w.N, w.K, rows=rows)
     stats = check_close16(got[rows], ref, w.K, MAXDQ, MAXDQ, "f16", "nvfp4 full size")
     assert stats["frac_exact"] > 0.9, stats
+
+
+# ---------------------------------------------------------------- split-K
+def run_splitk(g, a, b, sfa, sfb, M, N, K, k_splits):
+    c = g.gemm_nvfp4_bs_splitk(to_dev_u8(a), to_dev_u8(b), to_dev_u8(sfa), to_dev_u8(sfb),
+                               M, N, K, k_splits)
+    return bits16(c).reshape(M, N)
+
+
+@pytest.mark.parametrize("M,N,K,k_splits", [(128, 256, 1024, 3), (256, 512, 2048, 5),
+                                            (128, 384, 512, 64), (384, 128, 2304, 4)])
+def test_splitk_small(g, M, N, K, k_splits):
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", 1, M, N, K, 97 + M + K))
+    got = run_splitk(g, a, b, sfa, sfb, M, N, K, k_splits)
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, 1, M, N, K)
+    stats = check_close16(got, ref, K, MAXDQ, MAXDQ, "f16", f"nvfp4 split-K {M}x{N}x{K}/{k_splits}")
+    assert stats["max_ulp"] <= 1, stats
+
+
+def test_splitk_equals_unsplit_within_one_ulp(g):
+    M, N, K = 128, 512, 4096
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", 1, M, N, K, 98))
+    whole = run(g, a, b, sfa, sfb, 1, M, N, K)
+    split = run_splitk(g, a, b, sfa, sfb, M, N, K, 4)
+    d = np.abs(whole.astype(np.int32) - split.astype(np.int32))
+    assert d.max() <= 1, d.max()
+
+
+@pytest.mark.parametrize("name", sorted(synth.NVFP4_DECODE))
+def test_splitk_decode_shapes_sampled(g, name):
+    w, k_splits = synth.NVFP4_DECODE[name]
+    a, b, sfa, sfb = synth.nvfp4_inputs(w)
+    got = run_splitk(g, a, b, sfa, sfb, w.M, w.N, w.K, k_splits)
+    rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, w.L, w.M, w.N, w.K, rows=rows)
+    stats = check_close16(got[rows], ref, w.K, MAXDQ, MAXDQ, "f16", name)
+    assert stats["frac_exact"] > 0.9, stats
+
+
+def test_splitk_workspace_is_not_read(g):
+    # stale workspace contents must not leak into the result
+    M, N, K = 128, 256, 1024
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", 1, M, N, K, 99))
+    need = g.gemm_nvfp4_bs_splitk_workspace_bytes(M, N, K, 4)
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device="cuda")
+    c = g.gemm_nvfp4_bs_splitk(to_dev_u8(a), to_dev_u8(b), to_dev_u8(sfa), to_dev_u8(sfb),
+                               M, N, K, 4, workspace=ws)
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, 1, M, N, K)
+    check_close16(bits16(c).reshape(M, N), ref, K, MAXDQ, MAXDQ, "f16", "stale workspace")
