@@ -51,6 +51,7 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
   p.total_tiles = p.num_m_blocks * ((p.num_n_blocks + Cfg::MC - 1) / Cfg::MC);
+  p.group_m = raster_group_m(p.num_m_blocks, (long long)Cfg::TILE_M * K * 2);
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blocks;
   p.scale = scale;
@@ -92,6 +93,7 @@ static int run_bf16_splitk(const void* A, const void* B, float* ws, int M, int N
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
   p.total_tiles = p.num_m_blocks * p.num_n_blocks * splits;
+  p.group_m = raster_group_m(p.num_m_blocks, (long long)Cfg::TILE_M * K * 2);
   p.k_splits = splits;
   p.kb_per_split = kbps;
   p.status = dev.status;

@@ -88,6 +88,7 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = K / Cfg::BK;
   p.total_tiles = p.num_m_blocks * p.num_n_blocks * p.L;
+  p.group_m = raster_group_m(p.num_m_blocks, (long long)Cfg::TILE_M * (K / 2 + K / 16));
   p.k_splits = splits;
   p.kb_per_split = splits > 1 ? kb_per_split : p.num_k_blocks;
   p.rest_m = rest_m;

@@ -40,6 +40,19 @@ int encode_tmap_3d_strided(CUtensorMap* map, CUtensorMapDataType dtype, const vo
                            uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
                            CUtensorMapSwizzle swizzle);
 
+// Raster group height for the tile scheduler: consecutive work items walk
+// `group_m` M blocks down one N column before moving right, so the A rows of
+// a group are re-read from L2 across the N sweep and every B column block
+// is fetched once per group.  As many M blocks as keep the group's A rows
+// within 48 MB of the 129 MB L2 (all of them when A is small), at least 8.
+inline int raster_group_m(int num_m_blocks, long long a_bytes_per_m_block) {
+  const long long budget = 48ll << 20;
+  long long g = a_bytes_per_m_block > 0 ? budget / a_bytes_per_m_block : num_m_blocks;
+  if (g < 8) g = 8;
+  if (g > num_m_blocks) g = num_m_blocks;
+  return int(g < 1 ? 1 : g);
+}
+
 // Launchers; arguments are validated by the caller.
 int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
                      bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream);

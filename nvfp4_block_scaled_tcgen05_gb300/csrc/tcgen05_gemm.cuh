@@ -49,6 +49,7 @@ struct GemmParams {
   void* c_ptr;                    // output base (direct-store epilogue only)
   unsigned int* status;           // device status word
   unsigned long long timeout_ns;  // bound on every wait
+  int group_m;                    // M blocks per raster group (raster_group_m)
 };
 
 template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
@@ -136,7 +137,6 @@ struct TileCfg {
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
   static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * SF_WARPS;
-  static constexpr int GROUP_M = 8;
 
   // Instruction descriptor.  kind::f16: D=F32 (bits 4-5 = 1), A=B=BF16
   // (bits 7-9 = 1, 10-12 = 1), both K-major, N>>3 in bits 17-22, M>>4 in
@@ -161,10 +161,10 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int p
   const int per_batch = p.num_m_blocks * n_items;
   l = tile / per_batch;
   const int t = tile - l * per_batch;
-  const int group_tiles = Cfg::GROUP_M * n_items;
+  const int group_tiles = p.group_m * n_items;
   const int g = t / group_tiles;
-  const int first_m = g * Cfg::GROUP_M;
-  const int gm = min(p.num_m_blocks - first_m, Cfg::GROUP_M);
+  const int first_m = g * p.group_m;
+  const int gm = min(p.num_m_blocks - first_m, p.group_m);
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
   nb = (r / gm) * Cfg::MC + pair;
