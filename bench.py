@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-warm-s", type=float, default=0.6,
                     help="extra warm-up seconds so that clock samples cover the load")
-    ap.add_argument("--shapes", default="down,qkv,gqa,gqa_splitk,lora,router,nvfp4,nvfp4_decode",
+    ap.add_argument("--shapes", default="down,qkv,gqa,gateup_nn,gqa_splitk,lora,router,nvfp4,nvfp4_decode",
                     help="comma list of the extra shapes to measure")
     ap.add_argument("--no-headline", action="store_true",
                     help="profiling aid: measure only --shapes and print them")
@@ -491,6 +491,25 @@ def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
         tf = 2.0 * w.M * w.N * w.K / sec / 1e12
         out.append({"shape": name, "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
                     "frac_bf16_peak": tf / bf16_peak})
+        del As, Bs, Cs
+
+    if "gateup_nn" in which:
+        # NN layout (B stored [K][N]) on the gate/up shape
+        w = synth.BF16_WORKLOADS["gateup"]
+        A_h, B_h = synth.gemm_inputs(w)
+        Bkn_h = np.ascontiguousarray(B_h.T)
+        set_bytes = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
+        n = n_sets_for(set_bytes)
+        A0, B0 = up(A_h, torch.bfloat16), up(Bkn_h, torch.bfloat16)
+        As = [A0] + [A0.clone() for _ in range(n - 1)]
+        Bs = [B0] + [B0.clone() for _ in range(n - 1)]
+        Cs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        fn = lambda i: check(lib.gemm_bf16_nn(As[i].data_ptr(), Bs[i].data_ptr(), Cs[i].data_ptr(),
+                                              w.M, w.N, w.K, sp))
+        sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+        tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+        out.append({"shape": "gateup_nn", "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6,
+                    "TFLOP/s": tf, "frac_bf16_peak": tf / bf16_peak})
         del As, Bs, Cs
 
     if "gqa_splitk" in which:

@@ -64,6 +64,23 @@ extern "C" {
 GB300GEMM_API int gemm_bf16_nt(const void* A, const void* B, void* C, int M, int N, int K, void* stream);
 
 /*
+ * gemm_bf16_nn - C[M,N] = bf16( A[M,K] . B[K,N] ), the NN layout: B stored
+ * K rows of N (row-major [K][N]); FP32 accumulation on the tensor cores.
+ *
+ * Defined by: "sm121a_matmul.py", _sm121a_matmul_kernel and its docstring
+ * (A [M,K], B [K,N], FP32 accumulator, BF16 store).
+ *
+ *   A bf16 [M][K], B bf16 [K][N], C bf16 [M][N] (written), row-major;
+ *   M, N, K >= 1; K % 8 == 0 and N % 8 == 0 (16-byte row pitches); every
+ *   pointer 16-byte aligned; C must not overlap A or B.
+ * Results equal gemm_bf16_nt on the transposed B bit for bit (same tiles,
+ * same K order).
+ * Errors: GEMM_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARCH, _LAUNCH, _NO_DEVICE.
+ */
+GB300GEMM_API int gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int K,
+                               void* stream);
+
+/*
  * gemm_bf16_nt_scaled_acc - fused LoRA expand+fold:
  *     C[m,n] = bf16( float(C[m,n]) + scale * float(bf16(sum_k A[m,k] B[n,k])) )
  * The GEMM result is rounded to BF16 first, then multiplied by `scale` in

@@ -5,6 +5,7 @@ shared library is loaded on first call and must have been built (build.py)."""
 from .binding import (  # noqa: F401
     GemmError,
     bf16_scaled_add,
+    gemm_bf16_nn,
     gemm_bf16_nt,
     gemm_bf16_nt_ordered,
     gemm_bf16_nt_scaled_acc,

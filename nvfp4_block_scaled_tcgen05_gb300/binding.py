@@ -24,7 +24,7 @@ STATUS = {
     4: "GEMM_ERR_ALIAS", 5: "GEMM_ERR_ARCH", 6: "GEMM_ERR_LAUNCH", 7: "GEMM_ERR_TIMEOUT",
     8: "GEMM_ERR_NO_DEVICE",
 }
-EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
+EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nn", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
            "gemm_bf16_nt_splitk", "gemm_nvfp4_bs_splitk",
            "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
            "gemm_status_string")
@@ -53,6 +53,7 @@ def load() -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             vp, i, f, l = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_long
             lib.gemm_bf16_nt.argtypes = [vp, vp, vp, i, i, i, vp]
+            lib.gemm_bf16_nn.argtypes = [vp, vp, vp, i, i, i, vp]
             lib.gemm_bf16_nt_scaled_acc.argtypes = [vp, vp, vp, i, i, i, f, vp]
             lib.gemm_bf16_nt_ordered.argtypes = [vp, vp, vp, i, i, i, vp]
             lib.gemm_nvfp4_bs.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
@@ -120,6 +121,24 @@ def gemm_bf16_nt(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None
         raise ValueError("C must be [M, N]")
     _check(load().gemm_bf16_nt(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
                                _stream_ptr(stream)), "gemm_bf16_nt")
+    return C
+
+
+def gemm_bf16_nn(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, stream=None):
+    """C[M,N] = bf16(A[M,K] . B[K,N]) (B row-major [K][N]), FP32 accumulation."""
+    _mat(A, torch.bfloat16, "A")
+    _mat(B, torch.bfloat16, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"K mismatch: A {tuple(A.shape)} vs B {tuple(B.shape)}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _mat(C, torch.bfloat16, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C must be [M, N]")
+    _check(load().gemm_bf16_nn(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                               _stream_ptr(stream)), "gemm_bf16_nn")
     return C
 
 

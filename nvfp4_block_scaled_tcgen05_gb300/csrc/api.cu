@@ -166,6 +166,21 @@ int gemm_bf16_nt(const void* A, const void* B, void* C, int M, int N, int K, voi
   return launch_gemm_bf16(A, B, C, M, N, K, 0.0f, false, dev, static_cast<cudaStream_t>(stream));
 }
 
+int gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int K, void* stream) {
+  if (!A || !B || !C) return GEMM_ERR_NULL;
+  if (M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_SHAPE;
+  const long long tiles = (long long)((M + 127) / 128) * ((N + 63) / 64);
+  if (tiles > kMaxTiles) return GEMM_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_ALIGN;
+  if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_ALIGN;  // 16-byte row pitch of A, B and C
+  const size_t sa = size_t(M) * K * 2, sb = size_t(K) * N * 2, sc = size_t(M) * N * 2;
+  if (overlaps(C, sc, A, sa) || overlaps(C, sc, B, sb)) return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != GEMM_OK) return rc;
+  return launch_gemm_bf16_nn(A, B, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
+}
+
 int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_inout, int M, int N, int K,
                             float scale, void* stream) {
   int rc = check_bf16_nt(A, B, C_inout, M, N, K, 2);

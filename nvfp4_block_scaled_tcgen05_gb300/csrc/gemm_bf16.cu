@@ -23,6 +23,9 @@ using Bf16Pair = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;
 using Bf16Single = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2>;
 // plain BF16 output: 128-deep stages (8 MMAs per stage), 3 stages
 using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 1, 2>;
+// NN layout (B stored [K][N]): the same tiles with B staged MN-major
+using Bf16PairStoreNN = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 1, 2, true>;
+using Bf16SingleNN = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2, true, false, 1, 1, true>;
 // two pairs per cluster sharing (multicasting) their A rows
 using Bf16PairMC = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2, true, false, 2>;
 using Bf16PairStream = TileCfg<Operand::kBF16, 2, 256, 3, 4, 8>;
@@ -35,9 +38,14 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
   CUtensorMap ta, tb, tc;
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
                           64, Cfg::A_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc == GEMM_OK)
-    rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(K), uint64_t(N), 1,
-                        64, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == GEMM_OK) {
+    if constexpr (Cfg::B_MN)  // B [K][N]: boxes of 64 columns x BK rows
+      rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(N), uint64_t(K), 1,
+                          64, Cfg::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(K), uint64_t(N), 1,
+                          64, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, uint64_t(N), uint64_t(M), 1,
                         64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -120,6 +128,14 @@ int launch_gemm_bf16_splitk(const void* A, const void* B, void* C, float* ws, in
                          : run_bf16_splitk<Bf16Single>(A, B, ws, M, N, K, s_eff, kbps, dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_splitk_reduce(ws, C, size_t(M) * N, s_eff, dev, stream);
+}
+
+int launch_gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int K,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  int cg = (M > 128) ? 2 : 1;
+  if (const int o = cta_group_override()) cg = o;
+  return cg == 2 ? run_bf16<Bf16PairStoreNN>(A, B, C, M, N, K, 0.0f, false, dev, stream)
+                 : run_bf16<Bf16SingleNN>(A, B, C, M, N, K, 0.0f, false, dev, stream);
 }
 
 int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,

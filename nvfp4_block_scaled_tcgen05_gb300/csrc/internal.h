@@ -56,6 +56,9 @@ inline int raster_group_m(int num_m_blocks, long long a_bytes_per_m_block) {
 // Launchers; arguments are validated by the caller.
 int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
                      bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream);
+// NN layout: B [K][N] row-major.
+int launch_gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int K,
+                        const DeviceInfo& dev, cudaStream_t stream);
 int launch_gemm_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
                       int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_gemm_router(const void* A, const void* B, float* C, int M, int N, int K,

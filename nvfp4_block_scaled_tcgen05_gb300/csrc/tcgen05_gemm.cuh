@@ -53,7 +53,8 @@ struct GemmParams {
 };
 
 template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
-          bool SFA_REP_ = true, bool SFB_REP_ = false, int MC_ = 1, int KSUB_ = 1>
+          bool SFA_REP_ = true, bool SFB_REP_ = false, int MC_ = 1, int KSUB_ = 1,
+          bool B_MN_ = false>
 struct TileCfg {
   static constexpr Operand kOp = OP;
   static constexpr bool kFP4 = (OP == Operand::kNVFP4);
@@ -78,6 +79,10 @@ struct TileCfg {
   // issuer (barrier probe, release commit, bookkeeping) then has 1024 pipe
   // cycles to hide behind instead of 512.
   static constexpr int KSUB = KSUB_;
+  // B_MN: B is stored [K][N] (N contiguous, the NN layout).  Each stage holds
+  // the CTA's B columns as 64-column atoms (BK rows of 128 bytes each, the
+  // TMA's 128-byte swizzle), and the MMA reads B MN-major.
+  static constexpr bool B_MN = B_MN_;
   static constexpr int BK = kFP4 ? 256 : 64 * KSUB;  // K elements per stage
   static constexpr int KX = kFP4 ? 128 : 64;      // TMA x-extent per sub-tile (bytes or elements)
   static constexpr int MMA_K = kFP4 ? 64 : 16;    // K per MMA = 32 bytes per row
@@ -116,6 +121,8 @@ struct TileCfg {
   static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(MC == 1 || (MC == 2 && CG == 2 && !kFP4), "A multicast: BF16 CTA pairs only");
   static_assert(KSUB == 1 || (KSUB == 2 && !kFP4), "K sub-tiles: BF16 only");
+  static_assert(!B_MN || (!kFP4 && MC_ == 1 && B_ROWS % 64 == 0), "MN-major B: BF16, no multicast");
+  static constexpr int B_ATOM_BYTES = 64 * KSUB * 128;  // one 64-column MN-major atom of a stage
   static constexpr int A_SLICE_ROWS = BM / MC;    // A rows each CTA loads per stage
   static constexpr int A_SLICE_BYTES = A_SLICE_ROWS * 128;
   // the MMA issuer releases a stage only after the next stage's first MMA
@@ -145,7 +152,8 @@ struct TileCfg {
   __host__ __device__ static constexpr uint32_t idesc() {
     return kFP4 ? ((1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                    (uint32_t(TILE_M >> 4) << 24))
-                : ((1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                : ((1u << 4) | (1u << 7) | (1u << 10) | (B_MN ? (1u << 16) : 0u) |
+                   (uint32_t(BN >> 3) << 17) |
                    (uint32_t(TILE_M >> 4) << 24));
   }
 };
@@ -401,7 +409,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
               const uint32_t da = stage_a(stage) + sub * Cfg::A_SUB_BYTES;
               const uint32_t db = stage_b(stage) + sub * Cfg::B_SUB_BYTES;
-              if constexpr (kHintLoads) {
+              if constexpr (Cfg::B_MN) {
+                // B [K][N]: 64-column atoms of all BK rows, loaded once per stage
+                ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
+                if (sub == 0)
+#pragma unroll
+                  for (int at = 0; at < Cfg::B_ROWS / 64; ++at)
+                    ptx::tma_load_3d_hint(stage_b(stage) + at * Cfg::B_ATOM_BYTES, &tmap_b, fb,
+                                          b_row + 64 * at, kb * Cfg::BK, l, pol_ab);
+              } else if constexpr (kHintLoads) {
                 ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 ptx::tma_load_3d_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
               } else {
@@ -440,6 +456,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ptx::tma_load_3d_pair_mc(da + pair * Cfg::A_SLICE_BYTES, &tmap_a, fb, x,
                                          a_row + pair * Cfg::A_SLICE_ROWS, l, a_mask);
                 ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
+              } else if constexpr (Cfg::B_MN) {
+                ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
+                if (sub == 0)
+#pragma unroll
+                  for (int at = 0; at < Cfg::B_ROWS / 64; ++at)
+                    ptx::tma_load_3d_pair_hint(stage_b(stage) + at * Cfg::B_ATOM_BYTES, &tmap_b,
+                                               fb, b_row + 64 * at, kb * Cfg::BK, l, pol_ab);
               } else if constexpr (kHintLoads) {
                 ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
@@ -524,7 +547,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // the 14-bit start field (address >> 4) grows by that >> 4; shared
         // addresses stay below 2^18 bytes, so the field never carries over.
         const uint64_t adesc0 = ptx::sw128_kmajor_desc(stage_a(0));
-        const uint64_t bdesc0 = ptx::sw128_kmajor_desc(stage_b(0));
+        // MN-major B: leading offset = atom stride (next 64 columns), stride
+        // offset = 8 K rows (1024 bytes)
+        const uint64_t bdesc0 = Cfg::B_MN
+                                    ? ptx::smem_desc(stage_b(0), Cfg::B_ATOM_BYTES, 1024, 2)
+                                    : ptx::sw128_kmajor_desc(stage_b(0));
         while (ok) {
           const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
           const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
@@ -547,8 +574,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               // step j: K sub-tile j / 4, 32-byte K slice j % 4 within it
               const uint64_t ad =
                   adesc0 + soff + uint64_t(((j / 4) * Cfg::A_SUB_BYTES + 32 * (j % 4)) >> 4);
+              // K-major: sub-tile j / 4, 32-byte K slice j % 4; MN-major: rows 16 j ..
               const uint64_t bd =
-                  bdesc0 + soff + uint64_t(((j / 4) * Cfg::B_SUB_BYTES + 32 * (j % 4)) >> 4);
+                  Cfg::B_MN
+                      ? bdesc0 + soff + uint64_t((j * 16 * 128) >> 4)
+                      : bdesc0 + soff + uint64_t(((j / 4) * Cfg::B_SUB_BYTES + 32 * (j % 4)) >> 4);
               const uint32_t accum = !first_kb || (j != 0);
               if constexpr (kFP4)
                 ptx::mma_nvf4<CG>(d_tmem, ad, bd, idesc, sfa_t + 4 * j,

@@ -162,3 +162,15 @@ def test_nvfp4_splitk_rejects_bad_arguments(lib):
     assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P, 16, 1, 128, 256, 1024, 2, None) == 2  # small ws
     assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P + 8, big, 1, 128, 256, 1024, 2, None) == 3
     assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, P + 16, big, 1, 128, 256, 1024, 2, None) == 4  # ws on a
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, P, 2 * P, 8, 8, 8), 1),                 # NULL A
+    ((P, 2 * P, 3 * P, 0, 8, 8), 2),             # M = 0
+    ((P + 8, 2 * P, 3 * P, 8, 8, 8), 3),         # misaligned A
+    ((P, 2 * P, 3 * P, 8, 8, 12), 3),            # K % 8 != 0 (A pitch)
+    ((P, 2 * P, 3 * P, 8, 12, 8), 3),            # N % 8 != 0 (B and C pitch)
+    ((P, 2 * P, 2 * P + 16, 8, 8, 8), 4),        # C overlaps B
+])
+def test_gemm_bf16_nn_rejects_bad_arguments(lib, args, expect):
+    assert lib.gemm_bf16_nn(*args, None) == expect
