@@ -48,7 +48,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-warm-s", type=float, default=0.6,
                     help="extra warm-up seconds so that clock samples cover the load")
-    ap.add_argument("--shapes", default="down,qkv,gqa,gateup_nn,gqa_splitk,lora,router,nvfp4,nvfp4_decode",
+    ap.add_argument("--shapes",
+                    default="down,qkv,gqa,gateup_nn,gqa_splitk,down_streamk,qkv_streamk,lora,router,"
+                            "nvfp4,nvfp4_decode",
                     help="comma list of the extra shapes to measure")
     ap.add_argument("--no-headline", action="store_true",
                     help="profiling aid: measure only --shapes and print them")
@@ -515,6 +517,10 @@ def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
     if "gqa_splitk" in which:
         out.append(measure_splitk(torch, lib, synth, up, stream, dev, warmup, reps, check,
                                   bf16_peak, "gqa", 4))
+    for name in ("down", "qkv"):
+        if f"{name}_streamk" in which:
+            out.append(measure_streamk(torch, lib, synth, up, stream, dev, warmup, reps, check,
+                                       bf16_peak, name))
     if "lora" in which:
         out.append(measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check))
     if "router" in which:
@@ -552,6 +558,31 @@ def measure_splitk(torch, lib, synth, up, stream, dev, warmup, reps, check, bf16
     tf = 2.0 * w.M * w.N * w.K / sec / 1e12
     del As, Bs, Cs, Ws
     return {"shape": f"{name}_splitk{splits}", "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6,
+            "TFLOP/s": tf, "frac_bf16_peak": tf / bf16_peak}
+
+
+def measure_streamk(torch, lib, synth, up, stream, dev, warmup, reps, check, bf16_peak, name):
+    """Stream-K GEMM (GEMM with FP32 partial tiles + ordered fixup) on one shape;
+    the 160-tile shapes leave 8 tiles for a third round on 76 CTA pairs."""
+    import ctypes
+    sp = stream.cuda_stream
+    w = synth.BF16_WORKLOADS[name]
+    A_h, B_h = synth.gemm_inputs(w)
+    ws_bytes = int(lib.gemm_bf16_nt_streamk_workspace_bytes())
+    set_bytes = (w.M * w.K + w.N * w.K + w.M * w.N) * 2
+    n = n_sets_for(set_bytes)
+    A0, B0 = up(A_h, torch.bfloat16), up(B_h, torch.bfloat16)
+    As = [A0] + [A0.clone() for _ in range(n - 1)]
+    Bs = [B0] + [B0.clone() for _ in range(n - 1)]
+    Cs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)  # stream-ordered reuse
+    fn = lambda i: check(lib.gemm_bf16_nt_streamk(As[i].data_ptr(), Bs[i].data_ptr(),
+                                                  Cs[i].data_ptr(), ws.data_ptr(),
+                                                  ctypes.c_size_t(ws_bytes), w.M, w.N, w.K, sp))
+    sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+    del As, Bs, Cs, ws
+    return {"shape": f"{name}_streamk", "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6,
             "TFLOP/s": tf, "frac_bf16_peak": tf / bf16_peak}
 
 

@@ -128,6 +128,38 @@ GB300GEMM_API int gemm_bf16_nt_splitk(const void* A, const void* B, void* C, voi
 GB300GEMM_API size_t gemm_bf16_nt_splitk_workspace_bytes(int M, int N, int K, int k_splits);
 
 /*
+ * gemm_bf16_nt_streamk - BF16 NT GEMM, C = bf16(A . B^T), scheduled for
+ * shapes whose 256 x 256 tile count leaves part of the last wave idle.
+ * One cluster of two CTAs (one CTA pair) runs per co-resident slot, P of
+ * them.  The first floor(tiles / P) rounds of tiles are computed whole, as
+ * gemm_bf16_nt computes them.  The remaining tiles' 128-deep K iterations
+ * are dealt out evenly: pair p takes iterations [T*p/P, T*(p+1)/P) of the
+ * T left.  A tile whose iterations span several pairs is summed from their
+ * FP32 partial tiles in K order by a second kernel and rounded once to BF16;
+ * every other tile equals gemm_bf16_nt's bit for bit.
+ *
+ * Defined by: "gemm_dense.rs", dense_gemm_tc doc comment (the product) and
+ * dense_gemm_splitk doc comment (FP32 partial products over K chunks in a
+ * workspace, reduced to BF16); the work loop of persistent_block_scaled_gemm
+ * in "kernelbot-nvfp4-gemm-123329" (one program per slot striding over the
+ * tiles).  Dividing the last round's K iterations over every slot is this
+ * library's schedule; the pages have no such step.
+ *
+ *   A, B, C, M, N, K as for gemm_bf16_nt;  workspace: caller-owned device
+ *   memory of at least gemm_bf16_nt_streamk_workspace_bytes() bytes (one
+ *   size for every shape on the current device), 16-byte aligned, not
+ *   overlapping A, B or C; contents on entry ignored, on return unspecified.
+ * Errors: as gemm_bf16_nt; GEMM_ERR_SHAPE also for a workspace that is too
+ * small; GEMM_ERR_NULL for a NULL workspace.
+ */
+GB300GEMM_API int gemm_bf16_nt_streamk(const void* A, const void* B, void* C, void* workspace,
+                                       size_t workspace_bytes, int M, int N, int K, void* stream);
+
+/* Workspace bytes gemm_bf16_nt_streamk needs on the current device: two FP32
+ * 256 x 256 tiles per CTA pair of the device; 0 when no CUDA device is usable. */
+GB300GEMM_API size_t gemm_bf16_nt_streamk_workspace_bytes(void);
+
+/*
  * gemm_bf16_nt_splitk_static - gemm_bf16_nt_splitk without a workspace
  * argument, for callers that cannot allocate device memory: code whose host
  * framework owns the whole device pool and forbids other allocations,

@@ -11,6 +11,8 @@ from .binding import (  # noqa: F401
     gemm_bf16_nt_scaled_acc,
     gemm_bf16_nt_splitk,
     gemm_bf16_nt_splitk_workspace_bytes,
+    gemm_bf16_nt_streamk,
+    gemm_bf16_nt_streamk_workspace_bytes,
     gemm_nvfp4_bs_splitk,
     gemm_nvfp4_bs_splitk_workspace_bytes,
     gemm_get_device_status,

@@ -25,7 +25,7 @@ STATUS = {
     8: "GEMM_ERR_NO_DEVICE",
 }
 EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nn", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
-           "gemm_bf16_nt_splitk", "gemm_nvfp4_bs_splitk",
+           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk",
            "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
            "gemm_status_string")
 
@@ -61,6 +61,9 @@ def load() -> ctypes.CDLL:
             lib.gemm_bf16_nt_splitk.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
             lib.gemm_bf16_nt_splitk_workspace_bytes.argtypes = [i, i, i, i]
             lib.gemm_bf16_nt_splitk_workspace_bytes.restype = ctypes.c_size_t
+            lib.gemm_bf16_nt_streamk.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, vp]
+            lib.gemm_bf16_nt_streamk_workspace_bytes.argtypes = []
+            lib.gemm_bf16_nt_streamk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_nvfp4_bs_splitk.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                                  i, i, i, i, i, vp]
             lib.gemm_nvfp4_bs_splitk_workspace_bytes.argtypes = [i, i, i, i]
@@ -184,6 +187,34 @@ def gemm_bf16_nt_splitk(A: torch.Tensor, B: torch.Tensor, k_splits: int,
     _check(load().gemm_bf16_nt_splitk(A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                       workspace.data_ptr(), nbytes, M, N, K, int(k_splits),
                                       _stream_ptr(stream)), "gemm_bf16_nt_splitk")
+    return C
+
+
+def gemm_bf16_nt_streamk_workspace_bytes() -> int:
+    return int(load().gemm_bf16_nt_streamk_workspace_bytes())
+
+
+def gemm_bf16_nt_streamk(A: torch.Tensor, B: torch.Tensor, workspace: torch.Tensor | None = None,
+                         C: torch.Tensor | None = None, stream=None):
+    """C = bf16(A . B^T) on the stream-K schedule, with a caller workspace."""
+    _mat(A, torch.bfloat16, "A")
+    _mat(B, torch.bfloat16, "B")
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    if workspace is None:
+        need = gemm_bf16_nt_streamk_workspace_bytes()
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=A.device)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _mat(C, torch.bfloat16, "C")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().gemm_bf16_nt_streamk(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                       workspace.data_ptr(), nbytes, M, N, K,
+                                       _stream_ptr(stream)), "gemm_bf16_nt_streamk")
     return C
 
 

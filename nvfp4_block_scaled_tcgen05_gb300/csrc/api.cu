@@ -221,6 +221,31 @@ size_t gemm_bf16_nt_splitk_workspace_bytes(int M, int N, int K, int k_splits) {
   return size_t(s_eff) * size_t(M) * size_t(N) * 4;
 }
 
+int gemm_bf16_nt_streamk(const void* A, const void* B, void* C, void* workspace,
+                         size_t workspace_bytes, int M, int N, int K, void* stream) {
+  int rc = check_bf16_nt(A, B, C, M, N, K, 2);
+  if (rc != GEMM_OK) return rc;
+  if (N % 8 != 0) return GEMM_ERR_ALIGN;
+  if (!workspace) return GEMM_ERR_NULL;
+  if (!aligned16(workspace)) return GEMM_ERR_ALIGN;
+  // the whole buffer the caller hands over must be disjoint from the matrices
+  const size_t sa = size_t(M) * K * 2, sb = size_t(N) * K * 2, sc = size_t(M) * N * 2;
+  if (overlaps(workspace, workspace_bytes, A, sa) || overlaps(workspace, workspace_bytes, B, sb) ||
+      overlaps(workspace, workspace_bytes, C, sc))
+    return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  if (workspace_bytes < streamk_workspace_bytes(dev)) return GEMM_ERR_SHAPE;
+  return launch_gemm_bf16_streamk(A, B, C, static_cast<float*>(workspace), M, N, K, dev,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+size_t gemm_bf16_nt_streamk_workspace_bytes(void) {
+  DeviceInfo dev;
+  if (current_device(&dev) != GEMM_OK) return 0;
+  return streamk_workspace_bytes(dev);
+}
+
 int gemm_bf16_nt_ordered(const void* A, const void* B, float* C, int M, int N, int K,
                          void* stream) {
   int rc = check_bf16_nt(A, B, C, M, N, K, 4);

@@ -32,10 +32,12 @@ using Bf16PairStream = TileCfg<Operand::kBF16, 2, 256, 3, 4, 8>;
 using Bf16SingleStream = TileCfg<Operand::kBF16, 1, 256, 2, 4, 8>;
 constexpr int kStreamMaxK = 256;  // scaled-acc K up to this uses the streaming configurations
 
+// Tensor maps and schedule of a BF16 launch writing C = A.B^T (or its
+// scaled-acc update) tile by tile.
 template <class Cfg>
-static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
-                    bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
-  CUtensorMap ta, tb, tc;
+static int setup_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
+                      const DeviceInfo& dev, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tc,
+                      GemmParams& p) {
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
                           64, Cfg::A_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK) {
@@ -50,7 +52,7 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
     rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, uint64_t(N), uint64_t(M), 1,
                         64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != GEMM_OK) return rc;
-  GemmParams p{};
+  p = GemmParams{};
   p.M = M;
   p.N = N;
   p.K = K;
@@ -66,6 +68,16 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
   p.c_ptr = C;
   p.status = dev.status;
   p.timeout_ns = wait_timeout_ns();
+  return GEMM_OK;
+}
+
+template <class Cfg>
+static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
+                    bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
+  CUtensorMap ta, tb, tc;
+  GemmParams p;
+  const int rc = setup_bf16<Cfg>(A, B, C, M, N, K, scale, dev, ta, tb, tc, p);
+  if (rc != GEMM_OK) return rc;
   // the scale-factor maps are unused for BF16; pass A's map in their place
   if constexpr (Cfg::EPI_BUFS == 0) {
     return launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, ta, ta, p, dev, stream);
@@ -74,6 +86,192 @@ static int run_bf16(const void* A, const void* B, void* C, int M, int N, int K, 
                ? launch_tcgen05<Cfg, Epilogue::kScaledAccBF16>(ta, tb, tc, ta, ta, p, dev, stream)
                : launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, ta, ta, p, dev, stream);
   }
+}
+
+// Stream-K fixup plan, built on the host: for every tail tile whose K
+// iterations were divided over several clusters, its position and the
+// clusters c0 .. c0+n-1 that hold its partial tiles, in K order.  Cluster
+// c0's partial is its last segment (slot 1) unless its iteration range starts
+// at the tile's first iteration (slot 0); every later contributor's is its
+// first segment (slot 0).  Passed by value (about 3.3 KB of parameters).
+constexpr int kSkMaxTail = 256;
+struct StreamKPlan {
+  uint32_t mb[kSkMaxTail], nb[kSkMaxTail];  // output tile (M block, N block)
+  uint16_t c0[kSkMaxTail], n[kSkMaxTail];   // first contributing cluster, count (>= 2)
+  uint8_t slot0[kSkMaxTail];                // workspace slot of c0's partial
+  int tiles;                                // split tiles listed
+};
+
+// Stream-K fixup: a split tile is the FP32 sum of its partial tiles taken in
+// K order, rounded once to BF16 (tiles computed by one cluster were stored by
+// it).  Grid (split tiles, TILE_M / 4): 4 rows x 256 columns per CTA, 4
+// consecutive columns per thread, the loads of up to eight partials in flight
+// ahead of the ordered adds.  Launched as a programmatic dependent of the
+// GEMM: it is scheduled while the GEMM's last tiles run and waits for the
+// GEMM's completion in griddep_wait().
+constexpr int kFixupBatch = 8;
+template <class Cfg>
+__global__ void __launch_bounds__(256)
+    streamk_fixup_kernel(const __grid_constant__ StreamKPlan plan, const GemmParams p,
+                         const float* __restrict__ ws) {
+  static_assert(Cfg::BN == 256, "64 threads x 4 columns cover a row");
+  const int t = int(blockIdx.x);
+  const int c0 = plan.c0[t], n = plan.n[t];
+  const int r = int(blockIdx.y) * 4 + int(threadIdx.x) / 64;
+  const int col = (int(threadIdx.x) % 64) * 4;
+  const int grow = int(plan.mb[t]) * Cfg::TILE_M + r, gcol = int(plan.nb[t]) * Cfg::BN + col;
+  ptx::griddep_wait();
+  if (grow >= p.M || gcol >= p.N) return;
+  constexpr size_t kSlot = size_t(Cfg::TILE_M) * Cfg::BN;
+  const float* base = ws + size_t(r) * Cfg::BN + col;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < n; i += kFixupBatch) {
+    float4 v[kFixupBatch];
+#pragma unroll
+    for (int u = 0; u < kFixupBatch; ++u) {
+      const int k = i + u;  // contributor c0 + k
+      const size_t slot = size_t(c0 + k) * 2 + ((k == 0) ? plan.slot0[t] : 0);
+      if (k < n) v[u] = *reinterpret_cast<const float4*>(base + slot * kSlot);
+    }
+#pragma unroll
+    for (int u = 0; u < kFixupBatch; ++u) {
+      const int k = i + u;
+      if (k >= n) break;
+      if (k == 0) {
+        acc = v[u];
+      } else {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+  }
+  uint2 o;
+  o.x = pack_bf16x2(__float_as_uint(acc.x), __float_as_uint(acc.y));
+  o.y = pack_bf16x2(__float_as_uint(acc.z), __float_as_uint(acc.w));
+  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.c_ptr) + size_t(grow) * p.N + gcol) = o;
+}
+
+// The fixup plan of a stream-K launch (p.sk = P clusters sharing the tail of
+// T = (tiles mod C) * kbt iterations, P <= T): cluster c takes iterations
+// [T*c/P, T*(c+1)/P), so the owner of iteration x is ceil((x+1)*P/T) - 1.
+template <class Cfg>
+static void build_streamk_plan(const GemmParams& p, int C, StreamKPlan& plan) {
+  const int P = p.sk;
+  const int dp_rounds = p.total_tiles / C;
+  const int tail = p.total_tiles - dp_rounds * C;
+  const long long kbt = p.num_k_blocks;
+  const long long T = (long long)tail * kbt;
+  plan.tiles = 0;
+  for (int t = 0; t < tail; ++t) {
+    const long long ts = t * kbt, te = ts + kbt;
+    const int c0 = int(((ts + 1) * P + T - 1) / T - 1);
+    const int c1 = int((te * P + T - 1) / T - 1);
+    if (c1 == c0) continue;
+    int l, mb, nb;
+    decode_tile<Cfg>(dp_rounds * C + t, p, 0, l, mb, nb);
+    const int i = plan.tiles++;
+    plan.mb[i] = uint32_t(mb);
+    plan.nb[i] = uint32_t(nb);
+    plan.c0[i] = uint16_t(c0);
+    plan.n[i] = uint16_t(c1 - c0 + 1);
+    plan.slot0[i] = uint8_t((T * c0 / P == ts) ? 0 : 1);
+  }
+}
+
+// Clusters sharing the stream-K tail, or 0 for the data-parallel schedule.
+// Dividing the tail pays when the last round leaves most clusters idle: with
+// a quarter or more of them busy, GB300 runs the short round about as fast
+// per tile as a full one (measured), and the partial tiles cost more than
+// they save.  Among P = 1..C the host takes the P that minimises
+// ceil(T / P) K iterations on the critical path plus 0.1 iteration for each
+// partial tile written and summed (T / P + tail of them), the ratio measured
+// on the 5120 x 2048 x {2048, 11008} GEMMs.  GB300GEMM_SK_PAIRS=P (tests,
+// tuning) forces the division over min(P, C) clusters.
+static int streamk_share(int tiles, int kbt, int C) {
+  if (const char* e = std::getenv("GB300GEMM_SK_PAIRS")) {
+    const int v = std::atoi(e);
+    if (v >= 1) return v < C ? v : C;
+  }
+  const int tail = tiles % C;
+  if (tail == 0 || 4 * tail > C) return 0;
+  const long long T = (long long)tail * kbt;
+  int best = C;
+  double best_cost = 1e300;
+  for (int P = 1; P <= C; ++P) {
+    const double cost = double((T + P - 1) / P) + 0.1 * double(P + tail);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = P;
+    }
+  }
+  return best;
+}
+
+// Stream-K over exactly the co-resident cluster count C: floor(tiles / C)
+// data-parallel rounds of whole tiles, then the remaining tiles' K
+// iterations split evenly over P <= C clusters (each writes at most two
+// FP32 partial tiles to ws), then the ordered fixup of the split tiles.
+template <class Cfg>
+static int run_bf16_streamk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
+                            const DeviceInfo& dev, cudaStream_t stream) {
+  static_assert(!Cfg::kRegEpi && Cfg::EPI_BUFS > 0 && Cfg::MC == 1,
+                "partial tiles are written by the TMA-store epilogue of single-pair clusters");
+  CUtensorMap ta, tb, tc, tw;
+  GemmParams p;
+  int rc = setup_bf16<Cfg>(A, B, C, M, N, K, 0.0f, dev, ta, tb, tc, p);
+  if (rc != GEMM_OK) return rc;
+  const int clusters = tcgen05_cluster_capacity<Cfg, Epilogue::kStoreBF16>(dev);
+  if (clusters <= 0) return GEMM_ERR_LAUNCH;
+  if (size_t(clusters) > streamk_max_clusters(dev) || clusters > kSkMaxTail)
+    return GEMM_ERR_LAUNCH;
+  // workspace: [clusters * 2][TILE_M][BN] FP32, stored in 32 x 32 boxes
+  rc = encode_tmap_3d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, uint64_t(Cfg::BN),
+                      uint64_t(Cfg::TILE_M), uint64_t(clusters) * 2, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != GEMM_OK) return rc;
+  p.sk = streamk_share(p.total_tiles, p.num_k_blocks, clusters);
+  {
+    // no cluster without tail work: P <= T
+    const long long T = (long long)(p.total_tiles % clusters) * p.num_k_blocks;
+    if (p.sk > T) p.sk = int(T);
+  }
+  rc = launch_tcgen05<Cfg, Epilogue::kStoreBF16>(ta, tb, tc, tw, ta, p, dev, stream,
+                                                 p.sk ? clusters : 0);
+  if (rc != GEMM_OK) return rc;
+  if (p.sk == 0) return GEMM_OK;
+  static_assert(sizeof(StreamKPlan) + sizeof(GemmParams) + sizeof(void*) <= 4096,
+                "kernel parameters fit the classic 4 KB limit");
+  StreamKPlan plan;
+  build_streamk_plan<Cfg>(p, clusters, plan);
+  if (plan.tiles == 0) return GEMM_OK;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(plan.tiles, Cfg::TILE_M / 4);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* wsc = ws;
+  if (cudaLaunchKernelEx(&cfg, streamk_fixup_kernel<Cfg>, plan, p, wsc) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+size_t streamk_max_clusters(const DeviceInfo& dev) { return size_t(dev.num_sms / 2); }
+
+size_t streamk_workspace_bytes(const DeviceInfo& dev) {
+  return streamk_max_clusters(dev) * 2 * Bf16PairStore::TILE_M * Bf16PairStore::BN * sizeof(float);
+}
+
+int launch_gemm_bf16_streamk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
+                             const DeviceInfo& dev, cudaStream_t stream) {
+  return run_bf16_streamk<Bf16PairStore>(A, B, C, ws, M, N, K, dev, stream);
 }
 
 // Split-K: split s of the K blocks [s*kbps, (s+1)*kbps) writes its FP32

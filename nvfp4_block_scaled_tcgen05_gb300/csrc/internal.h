@@ -79,6 +79,12 @@ int nvfp4_splitk_effective_splits(int K, int splits, int* kb_per_split);
 int launch_gemm_nvfp4_splitk(const void* a, const void* b, const void* sfa, const void* sfb,
                              void* c, float* ws, int M, int N, int K, int splits,
                              const DeviceInfo& dev, cudaStream_t stream);
+// Stream-K (CTA pairs, 256 x 256 tiles): at most streamk_max_clusters(dev)
+// clusters, each with two FP32 partial tiles of workspace.
+size_t streamk_max_clusters(const DeviceInfo& dev);
+size_t streamk_workspace_bytes(const DeviceInfo& dev);
+int launch_gemm_bf16_streamk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
+                             const DeviceInfo& dev, cudaStream_t stream);
 // C[i] = bf16(sum_{s=0..S-1} ws[s*n + i]) in split order (_f16: FP16).
 int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
                          cudaStream_t stream);

@@ -70,6 +70,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream (launched
+// with programmatic stream serialization) be scheduled now; and, in that
+// kernel, wait until the preceding grid has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- L2 policies
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;

@@ -50,6 +50,7 @@ struct GemmParams {
   unsigned int* status;           // device status word
   unsigned long long timeout_ns;  // bound on every wait
   int group_m;                    // M blocks per raster group (raster_group_m)
+  int sk;                         // stream-K: clusters sharing the tail (0 = off)
 };
 
 template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
@@ -163,8 +164,8 @@ struct TileCfg {
 // `pair` takes the pair-th (which may lie past N: the pair then still loads
 // and multiplies, for its partner's sake, but stores nothing).
 template <class Cfg>
-__device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int pair, int& l,
-                                            int& mb, int& nb) {
+__host__ __device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int pair,
+                                                     int& l, int& mb, int& nb) {
   const int n_items = (p.num_n_blocks + Cfg::MC - 1) / Cfg::MC;
   const int per_batch = p.num_m_blocks * n_items;
   l = tile / per_batch;
@@ -172,10 +173,68 @@ __device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int p
   const int group_tiles = p.group_m * n_items;
   const int g = t / group_tiles;
   const int first_m = g * p.group_m;
-  const int gm = min(p.num_m_blocks - first_m, p.group_m);
+  const int gm = (p.num_m_blocks - first_m < p.group_m) ? p.num_m_blocks - first_m : p.group_m;
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
   nb = (r / gm) * Cfg::MC + pair;
+}
+
+// One work segment of a cluster: K blocks [kb0, kb1) of tile `tile`; slot
+// -1 = the whole tile (stored to C), 0 / 1 = a partial tile written as FP32
+// to the cluster's stream-K workspace slot (its first / last segment).
+struct Seg {
+  int tile, kb0, kb1, slot;
+};
+
+// Segment `idx` of cluster c among C clusters; false past the end.  Every
+// role of the kernel walks this same sequence.
+//  * plain / split-K: tile = c + idx*C; with split-K the batch slot of the
+//    tile selects its K blocks.
+//  * stream-K (p.sk = P): the first floor(tiles/C) rounds are whole tiles
+//    (tile = c + idx*C); the K iterations of the remaining tiles (the tail)
+//    are split evenly over clusters 0..P-1, cluster c taking iterations
+//    [T*c/P, T*(c+1)/P) in order, which makes at most its first and last
+//    segment partial.
+template <class Cfg>
+__device__ __forceinline__ bool seg_at(const GemmParams& p, int c, int C, int idx, Seg& s) {
+  if (!p.sk) {
+    const long long t = (long long)c + (long long)idx * C;
+    if (t >= p.total_tiles) return false;
+    s.tile = int(t);
+    s.slot = -1;
+    s.kb0 = 0;
+    s.kb1 = p.num_k_blocks;
+    if (p.k_splits > 1) {
+      int l, mb, nb;
+      decode_tile<Cfg>(s.tile, p, 0, l, mb, nb);
+      s.kb0 = l * p.kb_per_split;
+      s.kb1 = min(p.num_k_blocks, s.kb0 + p.kb_per_split);
+    }
+    return true;
+  }
+  const int dp_rounds = p.total_tiles / C;
+  if (idx < dp_rounds) {
+    s.tile = c + idx * C;
+    s.kb0 = 0;
+    s.kb1 = p.num_k_blocks;
+    s.slot = -1;
+    return true;
+  }
+  if (c >= p.sk) return false;
+  const long long kbt = p.num_k_blocks;
+  const long long T = (long long)(p.total_tiles - dp_rounds * C) * kbt;
+  const long long x0 = T * c / p.sk, x1 = T * (c + 1) / p.sk;
+  const int j = idx - dp_rounds;
+  const long long t = x0 / kbt + j;
+  const long long ts = t * kbt;  // first tail iteration of tail tile t
+  const long long lo = (j == 0) ? x0 : ts;
+  if (lo >= x1) return false;
+  const long long hi = min(x1, ts + kbt);
+  s.tile = dp_rounds * C + int(t);
+  s.kb0 = int(lo - ts);
+  s.kb1 = int(hi - ts);
+  s.slot = (s.kb0 == 0 && s.kb1 == kbt) ? -1 : (j == 0 ? 0 : 1);
+  return true;
 }
 
 // Converts 8 accumulator columns (v[0..7], FP32 bits) of one row and the
@@ -323,6 +382,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if constexpr (kFP4) {
       ptx::prefetch_tmap(&tmap_sfa);
       ptx::prefetch_tmap(&tmap_sfb);
+    } else if (p.sk) {
+      ptx::prefetch_tmap(&tmap_sfa);  // the stream-K workspace
+      // the fixup grid may be scheduled now; it waits for this grid's end
+      ptx::griddep_launch_dependents();
     }
   }
   if (warp == 1) {
@@ -383,9 +446,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // bit s: stage s has a load in flight / its parity
       bool ok = true;
-      for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters) {
+      Seg sg;
+      for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
         int l, mb, nb;
-        decode_tile<Cfg>(tile, p, pair, l, mb, nb);
+        decode_tile<Cfg>(sg.tile, p, pair, l, mb, nb);
         const int a_row = mb * Cfg::TILE_M + int(peer) * Cfg::BM;
         const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
         int sfb_atoms = 0;
@@ -393,8 +457,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t tx = uint32_t(CG) * (Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES +
                                             uint32_t(sfb_atoms) * Cfg::SFB_ATOM_BYTES);
         // split-K: l is the split; A and B are then single 2-D tensors (z = 0)
-        const int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
-        const int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
+        const int kb_begin = sg.kb0;
+        const int kb_end = sg.kb1;
         if (p.k_splits > 1) l = 0;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, w, 1)) {
@@ -527,18 +591,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int tile = cluster_id;
+      int idx = 0;             // this cluster's segment being multiplied
+      Seg sg;
       int pending_empty = -1;  // stage whose release commit is still to be issued
       // K tail: the last K block may need fewer than KSTEPS MMAs (the
       // zero-filled rest of its stage needs none)
       const int tail_kb = (p.K % Cfg::BK) ? p.K / Cfg::BK : -1;
       const int tail_steps = (p.K % Cfg::BK + Cfg::MMA_K - 1) / Cfg::MMA_K;
       constexpr int kPrep = Cfg::KSTEPS > 2 ? 1 : 0;  // MMA after which the next job is prepared
-      if (tile < p.total_tiles) {
-        int l, mb, nb;
-        decode_tile<Cfg>(tile, p, pair, l, mb, nb);
-        int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
-        int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
+      if (seg_at<Cfg>(p, cluster_id, num_clusters, 0, sg)) {
+        int kb_begin = sg.kb0;
+        int kb_end = sg.kb1;
         int kb = kb_begin;
         int it = 0, acc = 0;
         ok = wait_bar(acc_empty(0), 1u, w, 2) && wait_bar(ready_bar(0), 0u, w, 3);
@@ -562,7 +625,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           const int nstage = (stage + 1 == STAGES) ? 0 : stage + 1;
           const uint32_t nphase = (stage + 1 == STAGES) ? (phase ^ 1u) : phase;
           // the next job, filled in between this job's MMAs
-          int n_tile = tile, n_kb = kb + 1, n_kb_begin = kb_begin, n_kb_end = kb_end;
+          int n_idx = idx, n_kb = kb + 1, n_kb_begin = kb_begin, n_kb_end = kb_end;
           int n_it = it, n_acc = acc;
           bool has_next = true, next_ready = true;
           // (the full barrier orders the TMA data before these MMAs; no
@@ -590,13 +653,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
             if (j == kPrep) {
               if (last_kb) {
-                n_tile = tile + num_clusters;
-                has_next = n_tile < p.total_tiles;
+                Seg ns;
+                has_next = seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, ns);
                 if (has_next) {
-                  int l2, mb2, nb2;
-                  decode_tile<Cfg>(n_tile, p, pair, l2, mb2, nb2);
-                  n_kb_begin = (p.k_splits > 1) ? l2 * p.kb_per_split : 0;
-                  n_kb_end = min(p.num_k_blocks, n_kb_begin + p.kb_per_split);
+                  n_idx = idx + 1;
+                  n_kb_begin = ns.kb0;
+                  n_kb_end = ns.kb1;
                   n_kb = n_kb_begin;
                   n_it = it + 1;
                   n_acc = n_it % Cfg::NUM_ACC;
@@ -639,7 +701,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if constexpr (Cfg::SF_WARP) ptx::tc_fence_after();
           stage = nstage;
           phase = nphase;
-          tile = n_tile;
+          idx = n_idx;
           kb = n_kb;
           kb_begin = n_kb_begin;
           kb_end = n_kb_end;
@@ -666,12 +728,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       uint32_t last_phase = 0;
       bool ok = true;
       int job = 0;
-      for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters) {
-        int l, mb, nb;
-        decode_tile<Cfg>(tile, p, pair, l, mb, nb);
-        const int kb_begin = (p.k_splits > 1) ? l * p.kb_per_split : 0;
-        const int kb_end = min(p.num_k_blocks, kb_begin + p.kb_per_split);
-        for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
+      Seg sg;
+      for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++job) {
           if (job % Cfg::SF_WARPS == sfw) {
             if (!wait_bar(full_bar(stage), phase, w, 6)) {
               ok = false;
@@ -730,11 +789,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
     };
     // Look-ahead loads of the old output boxes of tile `t` into buffer half `half`.
-    auto prefetch_out = [&](int t, int half) {
+    auto prefetch_out = [&](const Seg& s2, int half) {
       if constexpr (kLookahead) {
         constexpr int NCH = Cfg::EPI_COLS / 64;
         int l2, mb2, nb2;
-        decode_tile<Cfg>(t, p, pair, l2, mb2, nb2);
+        decode_tile<Cfg>(s2.tile, p, pair, l2, mb2, nb2);
         const int r0 = mb2 * Cfg::TILE_M + int(peer) * Cfg::BM + q * 32;
         if (r0 >= p.M) return;
 #pragma unroll
@@ -750,21 +809,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
       }
     };
+    Seg sg;
     if constexpr (kLookahead) {
-      if (cluster_id < p.total_tiles) prefetch_out(cluster_id, 0);
+      if (seg_at<Cfg>(p, cluster_id, num_clusters, 0, sg)) prefetch_out(sg, 0);
     }
-    for (int tile = cluster_id; ok && tile < p.total_tiles; tile += num_clusters, ++it) {
+    for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx, ++it) {
       int l, mb, nb;
-      decode_tile<Cfg>(tile, p, pair, l, mb, nb);
+      decode_tile<Cfg>(sg.tile, p, pair, l, mb, nb);
       const int acc = it % Cfg::NUM_ACC;
       const uint32_t acc_phase = uint32_t(it / Cfg::NUM_ACC) & 1u;
       if constexpr (kLookahead) {
-        const int next = tile + num_clusters;
-        if (next < p.total_tiles) {
+        Seg ns;
+        if (seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, ns)) {
           // the stores of the previous tile read the other buffer half
           if (lane == 0) ptx::bulk_wait_group_read<0>();
           __syncwarp();
-          prefetch_out(next, (it + 1) & 1);
+          prefetch_out(ns, (it + 1) & 1);
         }
       }
       ok = __all_sync(0xffffffffu, wait_bar(acc_full(acc), acc_phase, w, 4));
@@ -942,6 +1002,35 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           ptx::tmem_ld_wait_regs(r1);
           if (c == Cfg::EPI_COLS / 64 - 1) release_acc(acc);
           if (!live) continue;
+          if constexpr (EPI == Epilogue::kStoreBF16 && !kFP4) {
+            if (sg.slot >= 0) {
+              // stream-K partial tile: two 32-column FP32 boxes into this
+              // cluster's workspace slot [cluster*2 + slot][TILE_M][BN] (its
+              // map takes the A-scale-factor map's place); the second box
+              // takes the next output buffer
+              const int sx = col_base + c * 64, sy = int(peer) * Cfg::BM + q * 32;
+              const int sz = int(cluster_id) * 2 + sg.slot;
+              write_box_row_f32(smem + (sbuf - sbase) + lane * 128, lane, r0);
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_3d(&tmap_sfa, sbuf, sx, sy, sz);
+                ptx::bulk_commit_group();
+              }
+              ++chunk_ctr;
+              const uint32_t sbuf2 = buf0 + int(chunk_ctr % Cfg::EPI_BUFS) * Cfg::EPI_BOX_BYTES;
+              if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
+              __syncwarp();
+              write_box_row_f32(smem + (sbuf2 - sbase) + lane * 128, lane, r1);
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_3d(&tmap_sfa, sbuf2, sx + 32, sy, sz);
+                ptx::bulk_commit_group();
+              }
+              continue;
+            }
+          }
           if constexpr (EPI == Epilogue::kScaledAccBF16) {
             const bool got = wait_bar(epi_bar(e, b), (epi_parity >> b) & 1u, w, 5);
             epi_parity ^= 1u << b;

@@ -174,3 +174,26 @@ def test_nvfp4_splitk_rejects_bad_arguments(lib):
 ])
 def test_gemm_bf16_nn_rejects_bad_arguments(lib, args, expect):
     assert lib.gemm_bf16_nn(*args, None) == expect
+
+
+def test_streamk_rejects_bad_arguments(lib):
+    f = lib.gemm_bf16_nt_streamk
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_size_t] + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    big = 1 << 20
+    assert f(0, 2 * P, 3 * P, 4 * P, big, 8, 8, 64, None) == 1            # NULL A
+    assert f(P, 2 * P, 3 * P, 0, big, 8, 8, 64, None) == 1                # NULL workspace
+    assert f(P, 2 * P, 3 * P, 4 * P, big, 0, 8, 64, None) == 2            # M = 0
+    assert f(P, 2 * P, 3 * P, 4 * P + 8, big, 8, 8, 64, None) == 3        # misaligned workspace
+    assert f(P, 2 * P, 3 * P, 4 * P, big, 8, 12, 64, None) == 3           # N % 8
+    assert f(P, 2 * P, 3 * P, P + 16, big, 8, 8, 64, None) == 4           # workspace overlaps A
+    assert f(P, 2 * P, 3 * P, 3 * P - 16, big, 8, 8, 64, None) == 4       # ... or C
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="a GPU is present")
+def test_streamk_workspace_without_a_gpu(lib):
+    ws = lib.gemm_bf16_nt_streamk_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws() == 0
+    f = lib.gemm_bf16_nt_streamk
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_size_t] + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    assert f(P, 2 * P, 3 * P, 8 * P, 1 << 20, 8, 8, 64, None) == 8
