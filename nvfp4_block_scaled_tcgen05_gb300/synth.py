@@ -18,6 +18,10 @@ problem sizes of the kernelbot submission):
 * ``router``  A[4510,2048], B[256,2048] ~ N(0,1) -> FP32
 * ``nvfp4``   L=1 M=4096 N=7168 K=16384; e2m1 codes uniform over all 16
   values (uniform bytes), scales 2^U{-4..2} stored as e4m3 bytes.
+* ``w4a16_qkvz`` A[1016,2048] ~ N(0,1) bf16 times NVFP4 weights [12288,2048]
+  (the qkvz projection at ISL 1016 of "gemm_dense.rs" w4a16_gemm_n128_m128):
+  e2m1 codes uniform, e4m3 block scales uniform over the codes of
+  2^-4 .. 2^2 (mantissas included), per-tensor scale 0.0123.
 """
 from __future__ import annotations
 
@@ -124,6 +128,36 @@ def gemm_inputs(w: Gemm, seed_offset: int = 0):
 def scaled_acc_out(M: int, N: int, seed: int) -> np.ndarray:
     """Initial values of the accumulated output, ~ N(0,1) bf16 bits."""
     return bf16_normal((M, N), 1.0, seed + 2)
+
+
+def e4m3_range_bytes(n: int, seed: int, lo: int = 0x18, hi: int = 0x48) -> np.ndarray:
+    """n e4m3 scale bytes uniform over the codes lo..hi (positive normals)."""
+    g = _gen(seed)
+    return torch.randint(lo, hi + 1, (int(n),), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+
+
+@dataclass(frozen=True)
+class W4a16:
+    name: str
+    M: int
+    N: int
+    K: int
+    scale2: float = 0.0123
+    seed: int = 1007
+
+
+W4A16 = {
+    "w4a16_qkvz": W4a16("w4a16_qkvz", 1016, 12288, 2048),
+}
+
+
+def w4a16_inputs(w: W4a16, seed_offset: int = 0):
+    """(A [M,K] bf16 bits, b [N,K/2] packed e2m1, sfb [N,K/16] e4m3 bytes, scale2)."""
+    s = w.seed + 17 * seed_offset
+    A = bf16_normal((w.M, w.K), 1.0, s)
+    b = uniform_bytes(w.N * w.K // 2, s + 1).reshape(w.N, w.K // 2)
+    sfb = e4m3_range_bytes(w.N * w.K // 16, s + 2).reshape(w.N, w.K // 16)
+    return A, b, sfb, float(np.float32(w.scale2))
 
 
 def nvfp4_inputs(w: Nvfp4, seed_offset: int = 0):

@@ -19,6 +19,9 @@ Each wrapper names the passage it follows:
 * ``gemm_nvfp4_bs``           - "kernelbot nvfp4 gemm submission 123329",
   sections "SCALE FACTORS", "NVIDIA Block layout", "Layout semantics" and
   ``custom_kernel``.
+* ``gemm_w4a16``              - "gemm_dense.rs" ``w4a16_gemm`` and its BF16
+  variant ``w4a16_gemm_n128_m128_bf16`` (NVFP4 weights dequantised to BF16,
+  FP32 accumulation); the layout and rounding readings are in ``oracle.c``.
 
 Parity pins for every function are in ``tests/test_oracle_pins.py``.
 """
@@ -90,6 +93,8 @@ def _load():
             lib.oracle_f64_to_f16_array.argtypes = [f64p, u16p, L]
             lib.oracle_gemm_nvfp4_bs.restype = I
             lib.oracle_gemm_nvfp4_bs.argtypes = [u8p, u8p, u8p, u8p, u16p, L, L, L, L, lp, L, I]
+            lib.oracle_gemm_w4a16.restype = I
+            lib.oracle_gemm_w4a16.argtypes = [u16p, u8p, u8p, F, u16p, L, L, L, lp, L, I]
             _lib = lib
     return _lib
 
@@ -235,3 +240,28 @@ def gemm_nvfp4_bs(a: np.ndarray, b: np.ndarray, sfa: np.ndarray, sfb: np.ndarray
                                       threads or default_threads())
     assert rc == 0, f"oracle_gemm_nvfp4_bs rc={rc}"
     return C
+
+
+def gemm_w4a16(A: np.ndarray, b: np.ndarray, sfb: np.ndarray, scale2: float, rows=None,
+               threads=None) -> np.ndarray:
+    """bf16 bits of C[rows] = bf16(fp32-sequential A[rows] @ w^T) with
+    w[n,k] = bf16(float(e2m1(b[n,k]) * e4m3(sfb[n,k/16])) * scale2).
+
+    A: uint16 bf16 bits [M,K]; b: uint8 [N,K/2] (low nibble = even k);
+    sfb: uint8 e4m3 [N,K/16]; scale2: the FP32 per-tensor scale.
+    """
+    A = _u16(A)
+    M, K = A.shape
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    sfb = np.ascontiguousarray(sfb, dtype=np.uint8)
+    N = b.shape[0]
+    assert b.size == N * K // 2 and sfb.size == N * K // 16
+    rp, nrows, _keep = _rows_arg(rows, M)
+    C = np.empty((nrows, N), dtype=np.uint16)
+    rc = _load().oracle_gemm_w4a16(_ptr(A, ctypes.c_uint16), _ptr(b, ctypes.c_uint8),
+                                   _ptr(sfb, ctypes.c_uint8), float(np.float32(scale2)),
+                                   _ptr(C, ctypes.c_uint16), M, N, K, rp, nrows,
+                                   threads or default_threads())
+    assert rc == 0, f"oracle_gemm_w4a16 rc={rc}"
+    return C
+

@@ -25,6 +25,8 @@
  *    custom_kernel: e2m1 values packed two per byte, one e4m3 scale per 16 K
  *    elements, scales stored as [32,4,rest_m,4,rest_k,L] with memory order
  *    l, tile_m, tile_k, g_m, i_m, i_k; FP16 output.
+ *  - "gemm_dense.rs", w4a16_gemm / w4a16_gemm_n128_m128_bf16: BF16
+ *    activations times NVFP4 weights dequantised to BF16, FP32 accumulation.
  *
  * Every function follows its definition literally: no blocking, no
  * reordering of the k sum, one output at a time.
@@ -260,19 +262,27 @@ static void bf16_row(void* vctx, long i) {
     free(arow);
 }
 
-static int run_bf16(const uint16_t* A, const uint16_t* B, void* out, long M, long N, long K,
-                    const long* rows, long nrows, int mode, float scale, int threads) {
-    if (M < 0 || N < 0 || K < 0) return -1;
+/* The row loop over a B already widened to float (bf16 values, exact). */
+static int run_bf16_widened(const uint16_t* A, const float* Bf, void* out, long M, long N,
+                            long K, const long* rows, long nrows, int mode, float scale,
+                            int threads) {
     if (!rows) nrows = M;
     for (long i = 0; rows && i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= M) return -2;
+    bf16_ctx c = {A, Bf, M, N, K, rows, mode, scale, out};
+    run_rows(bf16_row, &c, nrows, threads);
+    return 0;
+}
+
+static int run_bf16(const uint16_t* A, const uint16_t* B, void* out, long M, long N, long K,
+                    const long* rows, long nrows, int mode, float scale, int threads) {
+    if (M < 0 || N < 0 || K < 0) return -1;
     float* Bf = (float*)malloc(sizeof(float) * (size_t)(N * K > 0 ? N * K : 1));
     if (!Bf) return -3;
     for (long t = 0; t < N * K; ++t) Bf[t] = oracle_bf16_to_f32(B[t]);
-    bf16_ctx c = {A, Bf, M, N, K, rows, mode, scale, out};
-    run_rows(bf16_row, &c, nrows, threads);
+    int rc = run_bf16_widened(A, Bf, out, M, N, K, rows, nrows, mode, scale, threads);
     free(Bf);
-    return 0;
+    return rc;
 }
 
 /*
@@ -385,3 +395,46 @@ ORACLE_API int oracle_gemm_nvfp4_bs(const uint8_t* a, const uint8_t* b, const ui
     run_rows(nvfp4_row, &ctx, nrows, threads);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* W4A16: BF16 activations x NVFP4 weights.                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "gemm_dense.rs", w4a16_gemm doc comment: C = A @ dequant(B) with A [M,K]
+ * BF16 activations, B NVFP4 weights (e2m1 codes, FP8 e4m3 scales, an FP32
+ * per-tensor scale) and C [M,N] BF16; the doc comment of its BF16 variant
+ * (w4a16_gemm_n128_m128_bf16) names the math: FP4 dequantised to BF16, BF16
+ * products accumulated in FP32.
+ * Readings (the page gives no layout or rounding):
+ *  - b: N rows of K/2 bytes, element k in byte k/2, low nibble for even k
+ *    (the packing of the NVFP4 page); sfb: N rows of K/16 e4m3 bytes, byte
+ *    j of row n scaling elements 16j .. 16j+15 of row n;
+ *  - w[n,k] = bf16( float(e2m1(b[n,k]) * e4m3(sfb[n,k/16])) * scale2 ): the
+ *    code-times-scale product is exact in FP32, then one FP32 multiply by
+ *    the per-tensor scale and one rounding to BF16 (nearest, ties to even);
+ *  - C[m,n] = bf16( strict FP32 sum over k of A[m,k] * w[n,k] ), the same
+ *    accumulation as oracle_gemm_bf16_nt.
+ * Requires K % 16 == 0.  C is [nrows][N] bf16.
+ */
+ORACLE_API int oracle_gemm_w4a16(const uint16_t* A, const uint8_t* b, const uint8_t* sfb,
+                                 float scale2, uint16_t* C, long M, long N, long K,
+                                 const long* rows, long nrows, int threads) {
+    if (M < 0 || N < 0 || K < 0 || K % 16) return -1;
+    float* W = (float*)malloc(sizeof(float) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!W) return -3;
+    for (long n = 0; n < N; ++n) {
+        const uint8_t* brow = b + n * (K / 2);
+        for (long k = 0; k < K; ++k) {
+            double q = oracle_e2m1_decode(fp4_code(brow, k))
+                     * oracle_e4m3_decode(sfb[n * (K / 16) + k / 16]);
+            float qf = (float)q;            /* exact: at most 6 significant bits */
+            float wf = qf * scale2;         /* one FP32 rounding */
+            W[n * K + k] = oracle_bf16_to_f32(oracle_f32_to_bf16(wf));
+        }
+    }
+    int rc = run_bf16_widened(A, W, C, M, N, K, rows, nrows, 0, 0.0f, threads);
+    free(W);
+    return rc;
+}
+

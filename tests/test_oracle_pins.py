@@ -366,3 +366,109 @@ def test_nvfp4_fp16_overflow_to_inf():
     sf2 = np.full(L * M * K // 16, 0x50, dtype=np.uint8)  # scale 8.0 -> 64*48*48 = 147456 > 65504
     got2 = oracle.gemm_nvfp4_bs(a2, b, sf2, sf2, L, M, N, K)
     assert got2[0, 0] == 0x7c00
+
+
+# --------------------------------------------------------------------------
+# W4A16: BF16 activations x NVFP4 weights
+# --------------------------------------------------------------------------
+
+def _w4_one_weight(code: int, scale_byte: int, scale2: float) -> int:
+    """C[0,0] of a 1 x 1 x 16 W4A16 GEMM whose only nonzero product is
+    A[0,0] = 1 times weight (code, scale): the dequantised weight itself."""
+    A = np.zeros((1, 16), dtype=np.uint16)
+    A[0, 0] = 0x3F80
+    b = np.zeros((1, 8), dtype=np.uint8)
+    b[0, 0] = code & 0xF           # k = 0: low nibble
+    sfb = np.full((1, 1), scale_byte, dtype=np.uint8)
+    return int(oracle.gemm_w4a16(A, b, sfb, scale2)[0, 0])
+
+
+def test_w4a16_dequant_golden_examples():
+    with open(os.path.join(GOLDEN, "w4a16_dequant_examples.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 8
+    for code, sb, s2, want in rows:
+        scale2 = float(np.array([int(s2, 16)], dtype=np.uint32).view(np.float32)[0])
+        got = _w4_one_weight(int(code, 16), int(sb, 16), scale2)
+        assert got == int(want, 16), (code, sb, s2, hex(got), want)
+
+
+def test_w4a16_nibble_order_and_scale_groups():
+    # row 0 of b: k=0 -> 1.0 (code 2, low nibble of byte 0), k=1 -> 2.0 (code 4,
+    # high nibble), k=16 -> 1.0 (code 2) in scale group 1 (scale 2.0); group 0
+    # has scale 1.0.  One-hot rows of A pick out single weights.
+    K = 32
+    b = np.zeros((1, K // 2), dtype=np.uint8)
+    b[0, 0] = 0x42
+    b[0, 8] = 0x02
+    sfb = np.array([[0x38, 0x40]], dtype=np.uint8)
+    A = np.zeros((3, K), dtype=np.uint16)
+    A[0, 0] = A[1, 1] = A[2, 16] = 0x3F80
+    got = bf16_bits_to_f64(oracle.gemm_w4a16(A, b, sfb, 1.0)[:, 0])
+    assert got.tolist() == [1.0, 2.0, 2.0]
+
+
+@pytest.mark.parametrize("M,N,K,e2", [(7, 24, 64, 0), (33, 16, 160, -3), (5, 40, 32, 2)])
+def test_w4a16_exact_integers_match_integer_matmul(M, N, K, e2):
+    # scales 2.0 (0x40) make every e2m1 value times the scale an integer in
+    # {0, 1, 2, 3, 4, 6, 8, 12} up to sign; scale2 = 2^e2 keeps them exact, and
+    # small-integer activations keep every FP32 partial sum exact.
+    rng = np.random.default_rng(M * N + K)
+    A = synth.bf16_small_ints((M, K), -4, 4, M + K)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sfb = np.full((N, K // 16), 0x40, dtype=np.uint8)
+    tab = np.array(E2M1_TABLE)
+    codes = np.empty((N, K), dtype=np.uint8)
+    codes[:, 0::2] = b & 0xF
+    codes[:, 1::2] = b >> 4
+    w = (tab[codes] * 2.0 * 2.0**e2)
+    exact = bf16_bits_to_f64(A) @ w.T
+    got = oracle.gemm_w4a16(A, b, sfb, 2.0**e2)
+    assert np.array_equal(got, torch_bf16_bits(exact.astype(np.float32)))
+
+
+def test_w4a16_equals_bf16_gemm_on_torch_dequantised_weights():
+    # the dequantisation done by torch (float32 tensors, cast to bfloat16)
+    # followed by the pinned BF16 oracle GEMM gives the same bits
+    w = synth.W4a16("t", 37, 48, 96, 0.37, 91)
+    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+    tab = torch.tensor(E2M1_TABLE, dtype=torch.float32)
+    codes = torch.empty((w.N, w.K), dtype=torch.long)
+    bt = torch.from_numpy(b.astype(np.int64))
+    codes[:, 0::2] = bt & 0xF
+    codes[:, 1::2] = bt >> 4
+    sc = torch.from_numpy(sfb.copy()).view(torch.float8_e4m3fn).to(torch.float32)
+    q = tab[codes] * sc.repeat_interleave(16, dim=1)            # exact in float32
+    wq = (q * torch.tensor(scale2, dtype=torch.float32)).to(torch.bfloat16)
+    W = wq.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.gemm_w4a16(A, b, sfb, scale2), oracle.gemm_bf16_nt(A, W))
+
+
+def test_w4a16_within_fp32_bound_of_fp64():
+    w = synth.W4a16("t", 19, 40, 256, 0.0123, 92)
+    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+    tab = np.array(E2M1_TABLE)
+    codes = np.empty((w.N, w.K), dtype=np.uint8)
+    codes[:, 0::2] = b & 0xF
+    codes[:, 1::2] = b >> 4
+    sc = torch.from_numpy(sfb.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    wv = tab[codes] * np.repeat(sc, 16, axis=1) * scale2       # unrounded weights
+    a = bf16_bits_to_f64(A)
+    exact = a @ wv.T
+    got = bf16_bits_to_f64(oracle.gemm_w4a16(A, b, sfb, scale2))
+    # weight rounding (2^-9 relative) + FP32 accumulation (K * 2^-24) + output rounding
+    bound = (2.0**-9 + w.K * 2.0**-24) * (np.abs(a) @ np.abs(wv).T) + 2.0**-8 * np.abs(exact)
+    assert np.all(np.abs(got - exact) <= bound + 1e-30)
+    # and a wrong nibble order would break it
+    codes_sw = codes.copy()
+    codes_sw[:, 0::2], codes_sw[:, 1::2] = codes[:, 1::2], codes[:, 0::2]
+    wrong = a @ (tab[codes_sw] * np.repeat(sc, 16, axis=1) * scale2).T
+    assert not np.all(np.abs(got - wrong) <= bound + 1e-30)
+
+
+def test_w4a16_row_selection():
+    w = synth.W4a16("t", 21, 16, 64, 0.5, 93)
+    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+    full = oracle.gemm_w4a16(A, b, sfb, scale2)
+    rows = [20, 0, 7]
+    assert np.array_equal(oracle.gemm_w4a16(A, b, sfb, scale2, rows=rows), full[rows])
