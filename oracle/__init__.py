@@ -244,8 +244,8 @@ def gemm_nvfp4_bs(a: np.ndarray, b: np.ndarray, sfa: np.ndarray, sfb: np.ndarray
 
 def gemm_w4a16(A: np.ndarray, b: np.ndarray, sfb: np.ndarray, scale2: float, rows=None,
                threads=None) -> np.ndarray:
-    """bf16 bits of C[rows] = bf16(fp32-sequential A[rows] @ w^T) with
-    w[n,k] = bf16(float(e2m1(b[n,k]) * e4m3(sfb[n,k/16])) * scale2).
+    """bf16 bits of C[rows] = bf16(scale2 * fp32-sequential A[rows] @ w^T) with
+    the exact block-scaled weights w[n,k] = e2m1(b[n,k]) * e4m3(sfb[n,k/16]).
 
     A: uint16 bf16 bits [M,K]; b: uint8 [N,K/2] (low nibble = even k);
     sfb: uint8 e4m3 [N,K/16]; scale2: the FP32 per-tensor scale.

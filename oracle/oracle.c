@@ -222,7 +222,7 @@ typedef struct {
     const float* Bf;     /* [N][K] B widened to float (exact) */
     long M, N, K;
     const long* rows;    /* which rows of C to produce (NULL: 0..nrows-1) */
-    int mode;            /* 0: bf16 C, 1: scaled-acc, 2: fp32 router C */
+    int mode;            /* 0: bf16 C, 1: scaled-acc, 2: fp32 router C, 3: bf16(scale * sum) */
     float scale;
     void* out;           /* [nrows][N] */
 } bf16_ctx;
@@ -255,6 +255,10 @@ static void bf16_row(void* vctx, long i) {
             float t = c->scale * d;
             float r = oracle_bf16_to_f32(*o) + t;
             *o = oracle_f32_to_bf16(r);
+        } else if (c->mode == 3) {
+            /* one FP32 multiply of the sum, then one rounding to bf16 */
+            float t = c->scale * acc;
+            ((uint16_t*)c->out)[i * N + n] = oracle_f32_to_bf16(t);
         } else {
             ((float*)c->out)[i * N + n] = acc;
         }
@@ -410,11 +414,14 @@ ORACLE_API int oracle_gemm_nvfp4_bs(const uint8_t* a, const uint8_t* b, const ui
  *  - b: N rows of K/2 bytes, element k in byte k/2, low nibble for even k
  *    (the packing of the NVFP4 page); sfb: N rows of K/16 e4m3 bytes, byte
  *    j of row n scaling elements 16j .. 16j+15 of row n;
- *  - w[n,k] = bf16( float(e2m1(b[n,k]) * e4m3(sfb[n,k/16])) * scale2 ): the
- *    code-times-scale product is exact in FP32, then one FP32 multiply by
- *    the per-tensor scale and one rounding to BF16 (nearest, ties to even);
- *  - C[m,n] = bf16( strict FP32 sum over k of A[m,k] * w[n,k] ), the same
- *    accumulation as oracle_gemm_bf16_nt.
+ *  - the BF16 weight is the block-scaled value w[n,k] = e2m1(b[n,k]) *
+ *    e4m3(sfb[n,k/16]), which BF16 holds exactly (at most six significant
+ *    bits, magnitude in [2^-10, 2688]): the dequantisation rounds nothing;
+ *  - the per-tensor scale multiplies the FP32 sum once:
+ *    C[m,n] = bf16( scale2 * (strict FP32 sum over k of A[m,k] * w[n,k]) ),
+ *    the product rounded to FP32, then to BF16 (nearest, ties to even).
+ *    C = A @ dequant(B) is linear in scale2, so this is the same product
+ *    with one rounding where scaling every weight would add one per weight.
  * Requires K % 16 == 0.  C is [nrows][N] bf16.
  */
 ORACLE_API int oracle_gemm_w4a16(const uint16_t* A, const uint8_t* b, const uint8_t* sfb,
@@ -428,13 +435,10 @@ ORACLE_API int oracle_gemm_w4a16(const uint16_t* A, const uint8_t* b, const uint
         for (long k = 0; k < K; ++k) {
             double q = oracle_e2m1_decode(fp4_code(brow, k))
                      * oracle_e4m3_decode(sfb[n * (K / 16) + k / 16]);
-            float qf = (float)q;            /* exact: at most 6 significant bits */
-            float wf = qf * scale2;         /* one FP32 rounding */
-            W[n * K + k] = oracle_bf16_to_f32(oracle_f32_to_bf16(wf));
+            W[n * K + k] = (float)q;        /* exact */
         }
     }
-    int rc = run_bf16_widened(A, W, C, M, N, K, rows, nrows, 0, 0.0f, threads);
+    int rc = run_bf16_widened(A, W, C, M, N, K, rows, nrows, 3, scale2, threads);
     free(W);
     return rc;
 }
-

@@ -427,21 +427,33 @@ def test_w4a16_exact_integers_match_integer_matmul(M, N, K, e2):
     assert np.array_equal(got, torch_bf16_bits(exact.astype(np.float32)))
 
 
-def test_w4a16_equals_bf16_gemm_on_torch_dequantised_weights():
-    # the dequantisation done by torch (float32 tensors, cast to bfloat16)
-    # followed by the pinned BF16 oracle GEMM gives the same bits
-    w = synth.W4a16("t", 37, 48, 96, 0.37, 91)
-    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+def _torch_block_scaled(b, sfb, N, K):
+    """e2m1 * e4m3 weights from the format tables and torch's e4m3 cast (float32, exact)."""
     tab = torch.tensor(E2M1_TABLE, dtype=torch.float32)
-    codes = torch.empty((w.N, w.K), dtype=torch.long)
+    codes = torch.empty((N, K), dtype=torch.long)
     bt = torch.from_numpy(b.astype(np.int64))
     codes[:, 0::2] = bt & 0xF
     codes[:, 1::2] = bt >> 4
     sc = torch.from_numpy(sfb.copy()).view(torch.float8_e4m3fn).to(torch.float32)
-    q = tab[codes] * sc.repeat_interleave(16, dim=1)            # exact in float32
-    wq = (q * torch.tensor(scale2, dtype=torch.float32)).to(torch.bfloat16)
-    W = wq.view(torch.int16).numpy().view(np.uint16)
-    assert np.array_equal(oracle.gemm_w4a16(A, b, sfb, scale2), oracle.gemm_bf16_nt(A, W))
+    return tab[codes] * sc.repeat_interleave(16, dim=1)
+
+
+def test_w4a16_equals_bf16_gemm_on_torch_dequantised_weights():
+    # the block-scaled weights built by torch are exact in bf16; with
+    # scale2 = 1 the W4A16 oracle is the pinned BF16 oracle GEMM on them, and
+    # with any scale2 it is the pinned strict FP32 sum times scale2, rounded
+    # by torch's float32 multiply and bfloat16 cast
+    w = synth.W4a16("t", 37, 48, 96, 0.37, 91)
+    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+    q = _torch_block_scaled(b, sfb, w.N, w.K)
+    W = q.to(torch.bfloat16)
+    assert torch.equal(W.to(torch.float32), q)  # exact in bf16
+    W = W.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.gemm_w4a16(A, b, sfb, 1.0), oracle.gemm_bf16_nt(A, W))
+    acc = torch.from_numpy(oracle.gemm_router(A, W))
+    want = (acc * torch.tensor(scale2, dtype=torch.float32)).to(torch.bfloat16)
+    assert np.array_equal(oracle.gemm_w4a16(A, b, sfb, scale2),
+                          want.view(torch.int16).numpy().view(np.uint16))
 
 
 def test_w4a16_within_fp32_bound_of_fp64():
@@ -452,12 +464,12 @@ def test_w4a16_within_fp32_bound_of_fp64():
     codes[:, 0::2] = b & 0xF
     codes[:, 1::2] = b >> 4
     sc = torch.from_numpy(sfb.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
-    wv = tab[codes] * np.repeat(sc, 16, axis=1) * scale2       # unrounded weights
+    wv = tab[codes] * np.repeat(sc, 16, axis=1) * scale2
     a = bf16_bits_to_f64(A)
     exact = a @ wv.T
     got = bf16_bits_to_f64(oracle.gemm_w4a16(A, b, sfb, scale2))
-    # weight rounding (2^-9 relative) + FP32 accumulation (K * 2^-24) + output rounding
-    bound = (2.0**-9 + w.K * 2.0**-24) * (np.abs(a) @ np.abs(wv).T) + 2.0**-8 * np.abs(exact)
+    # FP32 accumulation (K * 2^-24), the FP32 scale product and the output rounding
+    bound = (w.K + 1) * 2.0**-24 * (np.abs(a) @ np.abs(wv).T) + 2.0**-8 * np.abs(exact)
     assert np.all(np.abs(got - exact) <= bound + 1e-30)
     # and a wrong nibble order would break it
     codes_sw = codes.copy()
