@@ -100,6 +100,38 @@ GB300GEMM_API int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_
                             float scale, void* stream);
 
 /*
+ * gemm_w4a16 - BF16 activations times NVFP4 weights:
+ *     w[n,k]  = e2m1(b[n,k]) * e4m3(sfb[n,k/16])          (exact in BF16)
+ *     C[m,n]  = bf16( scale2 * sum_k A[m,k] * w[n,k] ), FP32 accumulation
+ * The block-scaled weight has at most six significant bits, so its BF16
+ * form is exact; the per-tensor scale multiplies the FP32 sum once, then the
+ * result is rounded to BF16 (nearest, ties to even).  The weights are
+ * dequantised on chip, stage by stage, and never written out.
+ *
+ * Defined by: "gemm_dense.rs", w4a16_gemm doc comment (C = A @ dequant(B);
+ * A [M,K] BF16 activations; B NVFP4 packed weights: E2M1 codes, FP8 scales
+ * and an FP32 per-tensor scale; C [M,N] BF16) and the doc comment of
+ * w4a16_gemm_n128_m128_bf16 (FP4 dequantised to BF16, BF16 MMA, FP32
+ * accumulation).  The page gives no weight layout and no place for the
+ * per-tensor scale; this library reads the layout as HuggingFace-oriented
+ * rows (below) and applies the scale to the FP32 sum (C is linear in it).
+ *
+ *   A      bf16 [M][K], row pitch K                        (read)
+ *   b      uint8 [N][K/2]: element k of row n in byte k/2, low nibble for
+ *          even k, high nibble for odd k                   (read)
+ *   sfb    uint8 [N][K/16] e4m3: byte j of row n scales elements
+ *          16j .. 16j+15 of row n                          (read)
+ *   scale2 the FP32 per-tensor scale
+ *   C      bf16 [M][N] (written; must not overlap A, b or sfb)
+ *   M, N, K >= 1; K % 256 == 0 and N % 8 == 0 (16-byte rows of sfb, b and
+ *   C, which the tensor-memory-access copies need); every pointer 16-byte
+ *   aligned.
+ * Errors: GEMM_ERR_NULL, _SHAPE, _ALIGN, _ALIAS, _ARCH, _LAUNCH, _NO_DEVICE.
+ */
+GB300GEMM_API int gemm_w4a16(const void* A, const void* b, const void* sfb, float scale2, void* C,
+                             int M, int N, int K, void* stream);
+
+/*
  * gemm_bf16_nt_splitk - BF16 NT GEMM with the K dimension split into
  * `k_splits` chunks, for shapes with too few output tiles to fill the GPU:
  *     partial_s[m,n] = sum over the K blocks of split s of A[m,k] B[n,k]

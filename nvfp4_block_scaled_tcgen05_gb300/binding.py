@@ -25,7 +25,7 @@ STATUS = {
     8: "GEMM_ERR_NO_DEVICE",
 }
 EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nn", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
-           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk",
+           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk", "gemm_w4a16",
            "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
            "gemm_status_string")
 
@@ -62,6 +62,7 @@ def load() -> ctypes.CDLL:
             lib.gemm_bf16_nt_splitk_workspace_bytes.argtypes = [i, i, i, i]
             lib.gemm_bf16_nt_splitk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_bf16_nt_streamk.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, vp]
+            lib.gemm_w4a16.argtypes = [vp, vp, vp, f, vp, i, i, i, vp]
             lib.gemm_bf16_nt_streamk_workspace_bytes.argtypes = []
             lib.gemm_bf16_nt_streamk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_nvfp4_bs_splitk.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
@@ -215,6 +216,28 @@ def gemm_bf16_nt_streamk(A: torch.Tensor, B: torch.Tensor, workspace: torch.Tens
     _check(load().gemm_bf16_nt_streamk(A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                        workspace.data_ptr(), nbytes, M, N, K,
                                        _stream_ptr(stream)), "gemm_bf16_nt_streamk")
+    return C
+
+
+def gemm_w4a16(A: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor, scale2: float,
+               C: torch.Tensor | None = None, stream=None):
+    """C = bf16(scale2 * (A . w^T)), w = e2m1(b) * e4m3(sfb) (exact in bf16).
+
+    A bf16 [M,K]; b uint8 [N,K/2] packed e2m1 (low nibble = even k);
+    sfb uint8 [N,K/16] e4m3 block scales; C bf16 [M,N].
+    """
+    _mat(A, torch.bfloat16, "A")
+    _mat(b, torch.uint8, "b")
+    _mat(sfb, torch.uint8, "sfb")
+    M, K = A.shape
+    N = b.shape[0]
+    if tuple(b.shape) != (N, K // 2) or tuple(sfb.shape) != (N, K // 16):
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _mat(C, torch.bfloat16, "C")
+    _check(load().gemm_w4a16(A.data_ptr(), b.data_ptr(), sfb.data_ptr(), float(scale2),
+                             C.data_ptr(), M, N, K, _stream_ptr(stream)), "gemm_w4a16")
     return C
 
 

@@ -1,0 +1,56 @@
+// W4A16 GEMM: C[M,N] = bf16( scale2 * A[M,K] . w^T ), w = e2m1 * e4m3 the
+// NVFP4 weights of "gemm_dense.rs" w4a16_gemm (e2m1 codes, e4m3 block
+// scales, an FP32 per-tensor scale), on the persistent tcgen05 kernel: CTA
+// pairs, 256 x 256 tiles, 3 stages of 128 K values.  A is staged by TMA into
+// the stages; the packed codes and block scales by TMA into a 3-deep ring of
+// their own; eight warps per CTA turn the pair's 256 weight rows of each
+// stage into exact BF16 in the stage; the MMAs are the BF16 kind::f16 MMAs of the
+// dense GEMM; the epilogue multiplies the FP32 sum by scale2 once.  The
+// weights are read once per tile from L2/HBM at 4.5 bits each instead of 16.
+#include "launch.cuh"
+
+namespace gb300 {
+
+// direct-store epilogue (no output buffers): the shared memory holds the
+// code / scale ring instead
+using W4Pair = TileCfg<Operand::kW4A16, 2, 256, 3, 4, 0, true, false, 1, 2>;
+
+int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2, void* C,
+                      int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  using Cfg = W4Pair;
+  CUtensorMap ta, tcode, tscale, tc;
+  int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
+                          64, Cfg::A_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+  // codes: N rows of K/2 bytes, 64-byte x B_ROWS boxes (one K block of the
+  // CTA's weight rows); scales: N rows of K/16 bytes, 16-byte boxes
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tcode, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, uint64_t(K / 2), uint64_t(N),
+                        1, 64, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tscale, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb, uint64_t(K / 16),
+                        uint64_t(N), 1, 16, Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, uint64_t(N), uint64_t(M), 1,
+                        64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != GEMM_OK) return rc;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.L = 1;
+  p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
+  p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
+  p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
+  p.total_tiles = p.num_m_blocks * p.num_n_blocks;
+  p.group_m = raster_group_m(p.num_m_blocks, (long long)Cfg::TILE_M * K * 2);
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blocks;
+  p.scale = scale2;
+  p.c_ptr = C;
+  p.status = dev.status;
+  p.timeout_ns = wait_timeout_ns();
+  // the A-scale map is unused; pass A's map in its place
+  return launch_tcgen05<Cfg, Epilogue::kScaleBF16>(ta, tcode, tc, ta, tscale, p, dev, stream);
+}
+
+}  // namespace gb300

@@ -85,6 +85,10 @@ size_t streamk_max_clusters(const DeviceInfo& dev);
 size_t streamk_workspace_bytes(const DeviceInfo& dev);
 int launch_gemm_bf16_streamk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
                              const DeviceInfo& dev, cudaStream_t stream);
+// W4A16: C = bf16(scale2 * (A . w^T)), w[n,k] = e2m1(b[n,k]) * e4m3(sfb[n,k/16]);
+// b [N][K/2] (low nibble = even k), sfb [N][K/16]; K % 256 == 0, N % 8 == 0.
+int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2, void* C,
+                      int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 // C[i] = bf16(sum_{s=0..S-1} ws[s*n + i]) in split order (_f16: FP16).
 int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
                          cudaStream_t stream);

@@ -184,6 +184,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// The same arrive with the default (CTA-scope release) semantics, the form
+// cluster pipelines use for a consumer's per-stage signal to the other CTA
+// of a pair.  Measured on GB300: the cluster-scope release above costs the
+// issuing warp long enough that, issued every pipeline stage, it stalls the
+// pipeline; this form does not.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // TMA load whose completion is signalled on an mbarrier that may live in the
 // peer CTA of a CTA pair (bar is a shared::cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, uint32_t bar, int x,

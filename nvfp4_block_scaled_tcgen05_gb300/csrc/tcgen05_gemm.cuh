@@ -36,8 +36,15 @@
 
 namespace gb300 {
 
-enum class Operand : int { kBF16 = 0, kNVFP4 = 1 };
-enum class Epilogue : int { kStoreBF16 = 0, kScaledAccBF16 = 1, kStoreFP16 = 2, kStoreF32 = 3 };
+enum class Operand : int { kBF16 = 0, kNVFP4 = 1, kW4A16 = 2 };
+// kScaleBF16: C = bf16(scale * acc), one FP32 multiply then one rounding
+enum class Epilogue : int {
+  kStoreBF16 = 0,
+  kScaledAccBF16 = 1,
+  kStoreFP16 = 2,
+  kStoreF32 = 3,
+  kScaleBF16 = 4
+};
 
 struct GemmParams {
   int M, N, K, L;                 // K in elements
@@ -59,6 +66,9 @@ template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI
 struct TileCfg {
   static constexpr Operand kOp = OP;
   static constexpr bool kFP4 = (OP == Operand::kNVFP4);
+  // W4A16: BF16 MMAs whose B operand (NVFP4 weights) is dequantised into the
+  // stage by dedicated warps instead of being loaded by TMA.
+  static constexpr bool kW4 = (OP == Operand::kW4A16);
   static constexpr int CG = CG_;                  // CTAs per MMA (1 or 2)
   // MC = 2: a cluster of two CTA pairs computes two horizontally adjacent
   // tiles that share their A rows.  Each CTA loads half of its 128 A rows
@@ -139,12 +149,34 @@ struct TileCfg {
   // SF_WARPS = 2 the two warps take alternate stages.
   static constexpr int SF_WARPS = kFP4 ? 2 : 0;
   static constexpr bool SF_WARP = SF_WARPS > 0;
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], epi[W][B], mma_done, sf_full[S]
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1 + (SF_WARP ? STAGES : 0);
+  // W4A16: a second producer thread of each CTA TMA-loads its B rows'
+  // packed codes (64 bytes per row per 128-deep K block) and block scales
+  // (16 bytes per row: the scales of the even/odd pair of K blocks holding
+  // the block) into a RAW_STAGES-deep ring of its own, running ahead of the
+  // B stages; DQ_WARPS warps turn each job's codes into BF16 in the B stage
+  // and signal bq_full[stage] on the leader CTA (every warp of both CTAs
+  // arrives).  raw_full / raw_empty pace the ring.
+  static constexpr int DQ_WARPS = kW4 ? 8 : 0;
+  static constexpr int DQ_ROWS = kW4 ? B_ROWS / DQ_WARPS : 0;
+  static constexpr int RAW_STAGES = kW4 ? 3 : 0;
+  static constexpr int RAW_CODE_BYTES = kW4 ? B_ROWS * 64 : 0;  // codes of a job
+  static constexpr int RAW_BYTES = kW4 ? B_ROWS * (64 + 16) : 0;  // + the scale pairs
+  static constexpr int RAW_RING_BYTES = RAW_STAGES * RAW_BYTES;
+  static_assert(!kW4 || (KSUB == 2 && MC == 1 && !B_MN && DQ_ROWS % 8 == 0 && B_ROWS <= 256),
+                "W4A16: 128-deep stages, no multicast, K-major B");
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], epi[W][B], mma_done,
+  // sf_full[S] (NVFP4) or bq_full[S], raw_full[R], raw_empty[R] (W4A16)
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1 +
+                                  (SF_WARP ? STAGES : 0) + (kW4 ? STAGES + 2 * RAW_STAGES : 0);
   static constexpr int BAR_BYTES = NUM_BARS * 8 + 16;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + EPI_BYTES + RAW_RING_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * SF_WARPS;
+  // W4A16: one more warp issues the code / scale loads (a lane of the A
+  // producer's warp would share its stalls in barrier waits)
+  static constexpr int RAW_WARP = kW4 ? 2 + EPI_WARPS + DQ_WARPS : -1;
+  static constexpr int THREADS =
+      64 + 32 * EPI_WARPS + 32 * SF_WARPS + 32 * DQ_WARPS + (kW4 ? 32 : 0);
 
   // Instruction descriptor.  kind::f16: D=F32 (bits 4-5 = 1), A=B=BF16
   // (bits 7-9 = 1, 10-12 = 1), both K-major, N>>3 in bits 17-22, M>>4 in
@@ -247,6 +279,12 @@ __device__ __forceinline__ uint4 epi_chunk(const uint32_t* v, uint4 old, float s
     o.y = pack_bf16x2(v[2], v[3]);
     o.z = pack_bf16x2(v[4], v[5]);
     o.w = pack_bf16x2(v[6], v[7]);
+  } else if constexpr (EPI == Epilogue::kScaleBF16) {
+    uint32_t* q = &o.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      q[i] = pack_bf16x2(__float_as_uint(__fmul_rn(scale, __uint_as_float(v[2 * i]))),
+                         __float_as_uint(__fmul_rn(scale, __uint_as_float(v[2 * i + 1]))));
   } else if constexpr (EPI == Epilogue::kScaledAccBF16) {
     o.x = scaled_acc_bf16x2(old.x, pack_bf16x2(v[0], v[1]), scale);
     o.y = scaled_acc_bf16x2(old.y, pack_bf16x2(v[2], v[3]), scale);
@@ -293,6 +331,64 @@ __device__ __forceinline__ void write_box_row_f32(uint8_t* row, int lane, const 
   }
 }
 
+// W4A16 weights ("gemm_dense.rs", w4a16_gemm: C = A @ dequant(B), NVFP4
+// weights dequantised to BF16): 16 packed bytes of one weight row (32 e2m1
+// codes, element 2j in the low nibble of byte j) and the row's two e4m3
+// block scales for those elements (low byte: elements 0..15) ->
+//   w = e2m1 * e4m3
+// as 16 bf16x2 words in element order.  The product has at most six
+// significant bits and lies in [2^-10, 2688], so BF16 holds it exactly and
+// the BF16 multiply below rounds nothing (the per-tensor scale is applied
+// to the FP32 sum in the epilogue).
+//
+// The e2m1 code -> BF16 step is a byte-permute table lookup (integer pipe):
+// the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 of codes 0..7 are the BF16
+// patterns 0x0000 3F00 3F80 3FC0 4000 4040 4080 40C0; one PRMT looks up the
+// low bytes of four codes, one the high bytes, and the code's sign bit
+// (bit 3) becomes bit 15 of its BF16 value.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Four e2m1 codes (the low 16 bits of g, code i in bits 4i..4i+3) -> two
+// bf16x2 words (codes 0, 1 and codes 2, 3).
+__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t g, uint32_t& w01, uint32_t& w23) {
+  constexpr uint32_t kLo0 = 0xC0800000u, kLo1 = 0xC0804000u;  // low bytes, codes 0..3 / 4..7
+  constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;  // high bytes
+  const uint32_t sel = g & 0x7777u;
+  const uint32_t lo = prmt(kLo0, kLo1, sel);
+  uint32_t hi = prmt(kHi0, kHi1, sel);
+  // sign: a negative code selects byte 4 (0x80) in sign-replicate mode
+  // (0xFF), a positive one byte 4 as is (0x80); bit 6 then says which
+  const uint32_t sg = prmt(0u, 0x80u, (g & 0x8888u) | 0x4444u);
+  hi |= (sg << 1) & 0x80808080u;  // bit 7 of a byte: bit 6 of its sg byte
+  w01 = prmt(lo, hi, 0x5140u);
+  w23 = prmt(lo, hi, 0x7362u);
+}
+
+__device__ __forceinline__ void w4_dequant32(const uint4 raw, uint16_t sc2, uint32_t (&out)[16]) {
+  // the two block scales as bf16 (exact), each broadcast to both halves
+  uint32_t s16;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(sc2));
+  const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&s16));
+  const __nv_bfloat162 s0 = __float2bfloat162_rn(sf.x), s1 = __float2bfloat162_rn(sf.y);
+  const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t c[4];
+    e2m1x4_to_bf16(wd[i] & 0xFFFFu, c[0], c[1]);
+    e2m1x4_to_bf16(wd[i] >> 16, c[2], c[3]);
+    const __nv_bfloat162 sc = (i < 2) ? s0 : s1;  // elements 0..15 / 16..31
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 q = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&c[j]), sc);
+      out[4 * i + j] = *reinterpret_cast<const uint32_t*>(&q);
+    }
+  }
+}
+
 template <class Cfg, Epilogue EPI>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tcgen05_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -311,7 +407,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // registers with 16-byte global stores (frees shared memory for stages).
   constexpr bool kDirectStore = (Cfg::EPI_BUFS == 0);
   static_assert(!kDirectStore || EPI == Epilogue::kStoreBF16 || EPI == Epilogue::kStoreFP16 ||
-                    (EPI == Epilogue::kStoreF32 && Cfg::kRegEpi),
+                    EPI == Epilogue::kScaleBF16 || (EPI == Epilogue::kStoreF32 && Cfg::kRegEpi),
                 "direct stores serve the plain 16-bit epilogues and register-staged FP32 partials");
   // L2 policy hints: keep the operands resident (they are re-read by other
   // tiles), let the once-written output leave first.
@@ -322,7 +418,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                              ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t epi_base = sbase + STAGES * Cfg::STAGE_BYTES;
-  const uint32_t bar_base = epi_base + Cfg::EPI_BYTES;
+  const uint32_t raw_base = epi_base + Cfg::EPI_BYTES;  // W4A16 code / scale ring
+  const uint32_t bar_base = raw_base + Cfg::RAW_RING_BYTES;
   auto stage_a = [&](int s) { return sbase + s * Cfg::STAGE_BYTES; };
   auto stage_b = [&](int s) { return stage_a(s) + Cfg::A_BYTES; };
   auto stage_sfa = [&](int s) { return stage_b(s) + Cfg::B_BYTES; };
@@ -336,9 +433,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   };
   const uint32_t mma_done = bar_base + 8 * (2 * STAGES + 4 + Cfg::EPI_WARPS * Cfg::EPI_BUFS);
   auto sf_full = [&](int s) { return mma_done + 8 * (1 + s); };
+  auto bq_full = sf_full;  // W4A16 (which has no scale warps): B dequantised
+  auto raw_full = [&](int q) { return mma_done + 8 * (1 + STAGES + q); };  // W4A16 codes landed
+  auto raw_empty = [&](int q) {  // W4A16: every conversion warp has read slot q
+    return mma_done + 8 * (1 + STAGES + Cfg::RAW_STAGES + q);
+  };
   // the barrier that says stage s may be multiplied: its TMA data landed,
-  // and (NVFP4) its scales are in TMEM
-  auto ready_bar = [&](int s) { return Cfg::SF_WARP ? sf_full(s) : full_bar(s); };
+  // and (NVFP4) its scales are in TMEM, or (W4A16) its B is dequantised
+  auto ready_bar = [&](int s) { return (Cfg::SF_WARP || Cfg::kW4) ? sf_full(s) : full_bar(s); };
+  // W4A16: stage s may be multiplied once its A tiles landed (full) and its
+  // B rows were converted (bq_full); the MMA issuer waits on both itself
+  // (one wake-up per stage: a chain of waits through the conversion warps
+  // would add a second to every refill of the ring)
+  auto ready_probe = [&](int s, uint32_t ph) {
+    if constexpr (Cfg::kW4)
+      return ptx::mbar_test_wait(bq_full(s), ph) && ptx::mbar_test_wait(full_bar(s), ph);
+    else
+      return ptx::mbar_test_wait(ready_bar(s), ph);
+  };
+  auto ready_wait = [&](int s, uint32_t ph, const Watch& wt) {
+    if constexpr (Cfg::kW4)
+      return wait_bar(bq_full(s), ph, wt, 3) && wait_bar(full_bar(s), ph, wt, 3);
+    else
+      return wait_bar(ready_bar(s), ph, wt, 3);
+  };
   uint8_t* misc = smem + (bar_base - sbase) + 8 * Cfg::NUM_BARS;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(misc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(misc + 4);
@@ -372,6 +490,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     ptx::mbar_init(mma_done, 1);
     if constexpr (Cfg::SF_WARP)
       for (int s = 0; s < STAGES; ++s) ptx::mbar_init(sf_full(s), 1);
+    if constexpr (Cfg::kW4) {
+      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(bq_full(s), Cfg::DQ_WARPS * CG);
+      for (int q = 0; q < Cfg::RAW_STAGES; ++q) {
+        ptx::mbar_init(raw_full(q), 1);
+        ptx::mbar_init(raw_empty(q), Cfg::DQ_WARPS);
+      }
+    }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -382,6 +507,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if constexpr (kFP4) {
       ptx::prefetch_tmap(&tmap_sfa);
       ptx::prefetch_tmap(&tmap_sfb);
+    } else if constexpr (Cfg::kW4) {
+      ptx::prefetch_tmap(&tmap_sfb);  // the block scales (tmap_b: the codes)
     } else if (p.sk) {
       ptx::prefetch_tmap(&tmap_sfa);  // the stream-K workspace
       // the fixup grid may be scheduled now; it waits for this grid's end
@@ -454,8 +581,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
         int sfb_atoms = 0;
         if constexpr (kFP4) sfb_atoms = min(Cfg::SFB_ATOMS, p.rest_n - nb * Cfg::SFB_ATOMS);
-        const uint32_t tx = uint32_t(CG) * (Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES +
-                                            uint32_t(sfb_atoms) * Cfg::SFB_ATOM_BYTES);
+        const uint32_t tx =
+            uint32_t(CG) * (Cfg::A_BYTES + (Cfg::kW4 ? 0 : Cfg::B_BYTES) + Cfg::SFA_BYTES +
+                            uint32_t(sfb_atoms) * Cfg::SFB_ATOM_BYTES);
         // split-K: l is the split; A and B are then single 2-D tensors (z = 0)
         const int kb_begin = sg.kb0;
         const int kb_end = sg.kb1;
@@ -481,6 +609,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                   for (int at = 0; at < Cfg::B_ROWS / 64; ++at)
                     ptx::tma_load_3d_hint(stage_b(stage) + at * Cfg::B_ATOM_BYTES, &tmap_b, fb,
                                           b_row + 64 * at, kb * Cfg::BK, l, pol_ab);
+              } else if constexpr (Cfg::kW4) {
+                (void)db;
+                ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
               } else if constexpr (kHintLoads) {
                 ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 ptx::tma_load_3d_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
@@ -527,6 +658,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                   for (int at = 0; at < Cfg::B_ROWS / 64; ++at)
                     ptx::tma_load_3d_pair_hint(stage_b(stage) + at * Cfg::B_ATOM_BYTES, &tmap_b,
                                                fb, b_row + 64 * at, kb * Cfg::BK, l, pol_ab);
+              } else if constexpr (Cfg::kW4) {
+                (void)db;  // B is written by the dequantisation warps
+                ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
               } else if constexpr (kHintLoads) {
                 ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
@@ -574,6 +708,43 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         spin_ns(2000000ull);
       }
     }
+  } else if (Cfg::kW4 && warp == Cfg::RAW_WARP) {
+    if (lane == 0) {
+      // W4A16 codes and scales of this CTA's weight rows, job by job, into
+      // the raw ring (up to RAW_STAGES jobs ahead of the conversion warps):
+      // codes of K block kb, scales of the even/odd pair holding kb (the
+      // 16-byte TMA box starts at an even block)
+      int q = 0;
+      uint32_t qphase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      Seg sg;
+      for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
+        int l, mb, nb;
+        decode_tile<Cfg>(sg.tile, p, pair, l, mb, nb);
+        const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          if (!wait_bar(raw_empty(q), qphase ^ 1u, w, 10)) {
+            ok = false;
+            break;
+          }
+          const uint32_t slot = raw_base + q * Cfg::RAW_BYTES;
+          ptx::mbar_arrive_expect_tx(raw_full(q), Cfg::RAW_BYTES);
+          ptx::tma_load_3d(slot, &tmap_b, raw_full(q), kb * 64, b_row, 0);
+          ptx::tma_load_3d(slot + Cfg::RAW_CODE_BYTES, &tmap_sfb, raw_full(q), (kb & ~1) * 8,
+                           b_row, 0);
+          armed |= 1u << q;
+          armed_parity = (armed_parity & ~(1u << q)) | (qphase << q);
+          if (++q == Cfg::RAW_STAGES) {
+            q = 0;
+            qphase ^= 1u;
+          }
+        }
+      }
+      // every load must land before the CTA may exit
+      for (int r = 0; r < Cfg::RAW_STAGES; ++r)
+        if (armed & (1u << r)) drain_bar(raw_full(r), (armed_parity >> r) & 1u, w);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
@@ -604,7 +775,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int kb_end = sg.kb1;
         int kb = kb_begin;
         int it = 0, acc = 0;
-        ok = wait_bar(acc_empty(0), 1u, w, 2) && wait_bar(ready_bar(0), 0u, w, 3);
+        ok = wait_bar(acc_empty(0), 1u, w, 2) && ready_wait(0, 0u, w);
         ptx::tc_fence_after();
         // Stage s, MMA j: start address + s * STAGE_BYTES + offset of j, i.e.
         // the 14-bit start field (address >> 4) grows by that >> 4; shared
@@ -670,7 +841,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                   }
                 }
               }
-              if (has_next) next_ready = ptx::mbar_test_wait(ready_bar(nstage), nphase);
+              if (has_next) next_ready = ready_probe(nstage, nphase);
             }
           }
           if (last_kb) {
@@ -693,12 +864,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               ptx::tc_fence_after();
             }
           }
-          if (!next_ready && !wait_bar(ready_bar(nstage), nphase, w, 3)) {
+          if (!next_ready && !ready_wait(nstage, nphase, w)) {
             ok = false;
             break;
           }
-          // scales written by another thread: order them before the MMAs
-          if constexpr (Cfg::SF_WARP) ptx::tc_fence_after();
+          // scales / B written by other threads: order them before the MMAs
+          if constexpr (Cfg::SF_WARP || Cfg::kW4) ptx::tc_fence_after();
           stage = nstage;
           phase = nphase;
           idx = n_idx;
@@ -731,7 +902,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       Seg sg;
       for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
         for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++job) {
-          if (job % Cfg::SF_WARPS == sfw) {
+          if (job % (Cfg::SF_WARPS > 0 ? Cfg::SF_WARPS : 1) == sfw) {
             if (!wait_bar(full_bar(stage), phase, w, 6)) {
               ok = false;
               break;
@@ -757,7 +928,89 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // every copy must be complete before TMEM is released
       if (last >= 0) drain_bar(sf_full(last), last_phase, w);
     }
-  } else {
+  } else if (Cfg::kW4 && warp >= 2 + Cfg::EPI_WARPS && warp < Cfg::RAW_WARP) {
+    // ------------------------------------------------------------ W4A16 weights
+    // Warp d owns DQ_ROWS weight rows of this CTA's half of the tile and
+    // walks the same job sequence as the producers.  Per job: wait for its
+    // codes and scales in the raw ring, read this warp's rows into registers
+    // and hand the slot back, wait until the MMAs that last read the B stage
+    // are done, write the BF16 weights in the MMA's 128-byte-swizzled K-major
+    // layout, make the writes visible to the tensor core (async proxy) and
+    // arrive on the leader CTA's bq_full (the MMA issuer also waits for the
+    // stage's A tiles on full).
+    // Lanes: row prow (lane / 4) of an 8-row pass, K quarter kq (lane % 4).
+    // The lanes of quarters 2 and 3 convert their two 16-element halves in
+    // swapped order, which staggers the 16-byte chunks written together by
+    // an 8-lane phase over all eight bank groups of a 128-byte row.
+    constexpr int PASSES = Cfg::kW4 ? Cfg::DQ_ROWS / 8 : 1;
+    const int dw = warp - (2 + Cfg::EPI_WARPS);
+    const int prow = lane >> 2;
+    const int kq = lane & 3;
+    const int swap = kq & 2;  // 2: halves swapped
+    const uint32_t bq_target = (CG == 2) ? ptx::mapa_shared(bq_full(0), pair_leader) : bq_full(0);
+    int stage = 0, q = 0;
+    uint32_t phase = 0, qphase = 0;
+    bool ok = true;
+    Seg sg;
+    for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+        if (!__all_sync(0xffffffffu, wait_bar(raw_full(q), qphase, w, 8))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* slot = smem + (raw_base - sbase) + q * Cfg::RAW_BYTES;
+        uint4 codes[PASSES];
+        uint16_t scl[PASSES];
+#pragma unroll
+        for (int ps = 0; ps < PASSES; ++ps) {
+          const int r = dw * Cfg::DQ_ROWS + ps * 8 + prow;  // row within the CTA's B half
+          uint4 c = *reinterpret_cast<const uint4*>(slot + r * 64 + kq * 16);
+          uint16_t sv = *reinterpret_cast<const uint16_t*>(slot + Cfg::RAW_CODE_BYTES + r * 16 +
+                                                          (kb & 1) * 8 + kq * 2);
+          if (swap) {
+            c = make_uint4(c.z, c.w, c.x, c.y);
+            sv = uint16_t((sv >> 8) | (sv << 8));
+          }
+          codes[ps] = c;
+          scl[ps] = sv;
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(raw_empty(q));
+        if (++q == Cfg::RAW_STAGES) {
+          q = 0;
+          qphase ^= 1u;
+        }
+        if (!__all_sync(0xffffffffu, wait_bar(empty_bar(stage), phase ^ 1u, w, 11))) {
+          ok = false;
+          break;
+        }
+        const uint32_t sub_base = stage_b(stage) + (kq >> 1) * Cfg::B_SUB_BYTES;
+#pragma unroll
+        for (int ps = 0; ps < PASSES; ++ps) {
+          uint32_t v[16];
+          w4_dequant32(codes[ps], scl[ps], v);
+          const int r = dw * Cfg::DQ_ROWS + ps * 8 + prow;
+          uint8_t* rowp = smem + (sub_base - sbase) + r * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = ((kq & 1) << 2) + (i ^ swap);  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
+                make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2) ptx::mbar_arrive_remote(bq_target + 8 * stage);
+          else ptx::mbar_arrive(bq_full(stage));
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;          // epilogue warp index
     const int q = warp & 3;          // TMEM lane quarter this warp may access
@@ -973,7 +1226,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           for (int j = 0; j < 8; ++j) {
             if (col0 + 8 * j >= p.N) break;
             const uint32_t* v = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
-            const uint4 o = epi_chunk<EPI>(v, make_uint4(0, 0, 0, 0), 0.0f);
+            const uint4 o = epi_chunk<EPI>(v, make_uint4(0, 0, 0, 0), p.scale);
             *reinterpret_cast<uint4*>(dst + 8 * j) = o;
           }
         }

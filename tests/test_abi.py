@@ -197,3 +197,20 @@ def test_streamk_workspace_without_a_gpu(lib):
     f = lib.gemm_bf16_nt_streamk
     f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_size_t] + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     assert f(P, 2 * P, 3 * P, 8 * P, 1 << 20, 8, 8, 64, None) == 8
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, 2 * P, 3 * P, 1.0, 4 * P, 8, 8, 256), 1),         # NULL A
+    ((P, 2 * P, 0, 1.0, 4 * P, 8, 8, 256), 1),             # NULL scales
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 0, 8, 256), 2),         # M = 0
+    ((P, 2 * P + 8, 3 * P, 1.0, 4 * P, 8, 8, 256), 3),     # misaligned b
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 8, 8, 224), 3),         # K % 256 != 0
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 8, 12, 256), 3),        # N % 8 != 0
+    ((P, 2 * P, 3 * P, 1.0, 2 * P + 16, 8, 8, 256), 4),    # C overlaps b
+    ((P, 2 * P, 3 * P, 1.0, P + 16, 8, 8, 256), 4),        # C overlaps A
+])
+def test_w4a16_rejects_bad_arguments(lib, args, expect):
+    f = lib.gemm_w4a16
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.c_void_p] + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p]
+    assert f(*args, None) == expect
