@@ -6,8 +6,9 @@ step is one gemm_bf16_nt call (tile scheduler, TMA staging, tcgen05 MMA and
 BF16 epilogue) over one batch of synthetic inputs already resident in HBM.
 Consecutive steps rotate over several copies of the inputs and outputs so
 that the working set (> 2x L2) is never served from L2.  The other shapes of
-the same metric (down, qkv, gqa, the LoRA fold, the router and the NVFP4
-GEMM) are measured the same way and reported under "shapes".
+the same metric (down, qkv, gqa, their split-K / stream-K schedules, the
+NN layout, the W4A16 GEMM, the LoRA fold, the router and the NVFP4 GEMM)
+are measured the same way and reported under "shapes".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Prints one JSON line on rank 0.
@@ -49,8 +50,8 @@ def parse():
     ap.add_argument("--clock-warm-s", type=float, default=0.6,
                     help="extra warm-up seconds so that clock samples cover the load")
     ap.add_argument("--shapes",
-                    default="down,qkv,gqa,gateup_nn,gqa_splitk,down_streamk,qkv_streamk,lora,router,"
-                            "nvfp4,nvfp4_decode",
+                    default="down,qkv,gqa,gateup_nn,gqa_splitk,down_streamk,qkv_streamk,w4a16,lora,"
+                            "router,nvfp4,nvfp4_decode",
                     help="comma list of the extra shapes to measure")
     ap.add_argument("--no-headline", action="store_true",
                     help="profiling aid: measure only --shapes and print them")
@@ -521,6 +522,10 @@ def measure_shapes(torch, lib, synth, up, stream, dev, pk, warmup, reps, which):
         if f"{name}_streamk" in which:
             out.append(measure_streamk(torch, lib, synth, up, stream, dev, warmup, reps, check,
                                        bf16_peak, name))
+    for name in sorted(synth.W4A16):
+        if name in which or "w4a16" in which:
+            out.append(measure_w4a16(torch, lib, synth, up, stream, dev, warmup, reps, check,
+                                     bf16_peak, name))
     if "lora" in which:
         out.append(measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check))
     if "router" in which:
@@ -662,6 +667,28 @@ def measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_p
            "frac_fp4_mma_rate": tf / (fp4_peak * 4.0 / FP4_PEAK_RATIO)}
     del sets, cs
     return res
+
+
+def measure_w4a16(torch, lib, synth, up, stream, dev, warmup, reps, check, bf16_peak, name):
+    """W4A16 (BF16 activations x NVFP4 weights, converted on chip) on one shape.
+    The MMAs are BF16: reported against the BF16 tensor peak."""
+    sp = stream.cuda_stream
+    w = synth.W4A16[name]
+    A_h, b_h, sfb_h, scale2 = synth.w4a16_inputs(w)
+    set_bytes = A_h.size * 2 + b_h.size + sfb_h.size + w.M * w.N * 2
+    n = n_sets_for(set_bytes)
+    A0, b0, s0 = up(A_h, torch.bfloat16), up(b_h), up(sfb_h)
+    sets = [(A0, b0, s0)] + [(A0.clone(), b0.clone(), s0.clone()) for _ in range(n - 1)]
+    cs = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    fn = lambda i: check(lib.gemm_w4a16(sets[i][0].data_ptr(), sets[i][1].data_ptr(),
+                                        sets[i][2].data_ptr(), scale2, cs[i].data_ptr(),
+                                        w.M, w.N, w.K, sp))
+    sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    tf = 2.0 * w.M * w.N * w.K / sec / 1e12
+    del sets, cs
+    return {"shape": name, "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
+            "frac_bf16_peak": tf / bf16_peak,
+            "weight_bytes": int(b_h.size + sfb_h.size)}
 
 
 def measure_nvfp4_decode(torch, lib, synth, up, stream, dev, pk, warmup, reps, check, fp4_peak,
