@@ -2,11 +2,13 @@
 //
 //   C[l][m][n] = epilogue( sum_k A[l][m][k] * B[l][n][k] )      (NT layout)
 //
-// Operands: BF16 (kind::f16) or packed e2m1 with e4m3 block scales
-// (kind::mxf4nvf4, scale_vec::4X).  A CTA group (one CTA, or a pair of CTAs
-// on two SMs running cta_group::2 MMAs) walks the output tiles
-// tile = cluster + i * clusters in grouped-M raster order.  A tile is
-// (128 * CG) x BN; each CTA stages its own 128 rows of A and BN/CG rows of B.
+// Operands: BF16 (kind::f16), packed e2m1 with e4m3 block scales
+// (kind::mxf4nvf4, scale_vec::4X), or BF16 A with packed e2m1 B converted
+// to BF16 on chip (W4A16, kind::f16).  A CTA group (one CTA, or a pair of
+// CTAs on two SMs running cta_group::2 MMAs) walks the output tiles
+// tile = cluster + i * clusters in grouped-M raster order (seg_at: also the
+// split-K and stream-K schedules).  A tile is (128 * CG) x BN; each CTA
+// stages its own 128 rows of A and BN/CG rows of B.
 // Roles per CTA:
 //   warp 0        TMA producer: A/B tiles (128-byte swizzle) and, for NVFP4,
 //                 the 512-byte scale atoms, into a STAGES-deep smem ring;
@@ -19,7 +21,9 @@
 //                 epilogue warps ("register-staged") every accumulator column
 //                 is read into registers before the accumulator is released,
 //                 so a single TMEM accumulator still overlaps the epilogue
-//                 with the next tile's MMAs.
+//                 with the next tile's MMAs;
+//   W4A16 only    8 conversion warps (packed codes -> BF16 B stages) and
+//                 one warp TMA-loading the codes and scales into a ring.
 // Every wait is bounded (globaltimer); a timeout records a code in the
 // device status word, raises a CTA-wide abort flag, drains in-flight copies
 // and MMAs, frees TMEM and returns.
@@ -149,7 +153,7 @@ struct TileCfg {
   // SF_WARPS = 2 the two warps take alternate stages.
   static constexpr int SF_WARPS = kFP4 ? 2 : 0;
   static constexpr bool SF_WARP = SF_WARPS > 0;
-  // W4A16: a second producer thread of each CTA TMA-loads its B rows'
+  // W4A16: a producer warp of each CTA (RAW_WARP) TMA-loads its B rows'
   // packed codes (64 bytes per row per 128-deep K block) and block scales
   // (16 bytes per row: the scales of the even/odd pair of K blocks holding
   // the block) into a RAW_STAGES-deep ring of its own, running ahead of the
@@ -172,8 +176,7 @@ struct TileCfg {
   static constexpr int SMEM_BYTES =
       1024 + STAGES * STAGE_BYTES + EPI_BYTES + RAW_RING_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
-  // W4A16: one more warp issues the code / scale loads (a lane of the A
-  // producer's warp would share its stalls in barrier waits)
+  // W4A16: the warp that issues the code / scale loads
   static constexpr int RAW_WARP = kW4 ? 2 + EPI_WARPS + DQ_WARPS : -1;
   static constexpr int THREADS =
       64 + 32 * EPI_WARPS + 32 * SF_WARPS + 32 * DQ_WARPS + (kW4 ? 32 : 0);
