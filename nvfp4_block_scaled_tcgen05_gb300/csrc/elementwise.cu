@@ -7,6 +7,7 @@
 
 #include "epilogue_math.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gb300 {
 
@@ -50,6 +51,9 @@ template <bool kF16>
 __global__ void __launch_bounds__(kThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, uint16_t* __restrict__ C, size_t n,
                          int splits) {
+  // launched as a programmatic dependent of the split-K GEMM: wait for its
+  // end (and its partials) here, after this grid's launch overlapped it
+  ptx::griddep_wait();
   const size_t nvec = n / 8;
   const size_t stride = size_t(gridDim.x) * kThreads;
   for (size_t i = size_t(blockIdx.x) * kThreads + threadIdx.x; i < nvec; i += stride) {
@@ -81,24 +85,37 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
-int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
-                         cudaStream_t stream) {
+template <bool kF16>
+int launch_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
+                  cudaStream_t stream) {
   const size_t nvec = n / 8;
   const size_t want = (nvec + kThreads - 1) / kThreads;
   const int grid = int(std::max<size_t>(1, std::min<size_t>(want, size_t(dev.num_sms) * 8)));
-  splitk_reduce_kernel<false><<<grid, kThreads, 0, stream>>>(ws, static_cast<uint16_t*>(C), n,
-                                                             splits);
-  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t* out = static_cast<uint16_t*>(C);
+  if (cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<kF16>, ws, out, n, splits) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
+                         cudaStream_t stream) {
+  return launch_reduce<false>(ws, C, n, splits, dev, stream);
 }
 
 int launch_splitk_reduce_f16(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
                              cudaStream_t stream) {
-  const size_t nvec = n / 8;
-  const size_t want = (nvec + kThreads - 1) / kThreads;
-  const int grid = int(std::max<size_t>(1, std::min<size_t>(want, size_t(dev.num_sms) * 8)));
-  splitk_reduce_kernel<true><<<grid, kThreads, 0, stream>>>(ws, static_cast<uint16_t*>(C), n,
-                                                            splits);
-  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+  return launch_reduce<true>(ws, C, n, splits, dev, stream);
 }
 
 int launch_scaled_add(void* out, const void* d, float scale, long n, const DeviceInfo& dev,

@@ -514,9 +514,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       ptx::prefetch_tmap(&tmap_sfb);  // the block scales (tmap_b: the codes)
     } else if (p.sk) {
       ptx::prefetch_tmap(&tmap_sfa);  // the stream-K workspace
-      // the fixup grid may be scheduled now; it waits for this grid's end
-      ptx::griddep_launch_dependents();
     }
+    // split-K / stream-K: the reduce or fixup grid may be scheduled now; it
+    // waits for this grid's end
+    if (p.sk || p.k_splits > 1) ptx::griddep_launch_dependents();
   }
   if (warp == 1) {
     ptx::tmem_alloc<CG>(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), Cfg::TMEM_COLS);
