@@ -18,10 +18,11 @@
 //   warps 2..     epilogue: tcgen05.ld -> convert (bf16 / fp16 / scaled-acc)
 //                 -> swizzled smem box -> TMA store; for scaled-acc the old
 //                 output box is TMA-loaded into the same smem first.  With 8
-//                 epilogue warps ("register-staged") every accumulator column
-//                 is read into registers before the accumulator is released,
-//                 so a single TMEM accumulator still overlaps the epilogue
-//                 with the next tile's MMAs;
+//                 epilogue warps and a single TMEM accumulator
+//                 ("register-staged") every accumulator column is read into
+//                 registers before the accumulator is released, so the
+//                 epilogue still overlaps the next tile's MMAs; with two
+//                 accumulators 8 warps take half of the columns each;
 //   W4A16 only    8 conversion warps (packed codes -> BF16 B stages) and
 //                 one warp TMA-loading the codes and scales into a ring.
 // Every wait is bounded (globaltimer); a timeout records a code in the
@@ -87,7 +88,6 @@ struct TileCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static constexpr int EPI_BUFS = EPI_BUFS_;
-  static constexpr bool kRegEpi = (EPI_WARPS == 8);
   static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue warp
   // KSUB = 2 (BF16): a stage holds two 64-deep K sub-tiles per operand (two
   // TMA boxes each), i.e. 8 MMAs per stage.  The per-stage work of the MMA
@@ -130,6 +130,10 @@ struct TileCfg {
   static constexpr int SF_COLS = kFP4 ? KSTEPS * 4 * (1 + SFB_ATOMS) : 0;
   static constexpr int NUM_ACC = (2 * BN + STAGES * SF_COLS <= 512) ? 2 : 1;
   static constexpr int SF_TMEM_BASE = NUM_ACC * BN;
+  // 8 epilogue warps with a single accumulator ("register-staged"): every
+  // accumulator column is read into registers before the accumulator is
+  // released; with two accumulators 8 warps split the columns in halves
+  static constexpr bool kRegEpi = (EPI_WARPS == 8) && (NUM_ACC == 1);
   static constexpr int TMEM_COLS = 512;
   static_assert(NUM_ACC * BN + STAGES * SF_COLS <= TMEM_COLS, "TMEM column budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
