@@ -131,3 +131,19 @@ def test_streamk_rejects_a_small_workspace(g, ws):
     B = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(g.GemmError):
         g.gemm_bf16_nt_streamk(A, B, ws[:1024])
+
+
+def _random_shapes(seed, count):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 1600)), int(rng.integers(1, 260)) * 8, int(rng.integers(1, 400)) * 8)
+            for _ in range(count)]
+
+
+@pytest.mark.parametrize("M,N,K", _random_shapes(2024, 6))
+def test_streamk_random_shapes_exact_integers(g, ws, share, M, N, K):
+    # seeded ragged shapes, every sum an exact integer: bit-exact for any
+    # division of the tail
+    A = synth.bf16_small_ints((M, K), -2, 2, M + 3 * K)
+    B = synth.bf16_small_ints((N, K), -2, 2, N + 5 * K)
+    C = g.gemm_bf16_nt_streamk(to_dev_bf16(A), to_dev_bf16(B), ws)
+    check_bitexact16(bits16(C), oracle.gemm_bf16_nt(A, B), f"stream-K random {M}x{N}x{K}")

@@ -123,3 +123,21 @@ def test_w4a16_full_size_sampled(g):
     ref = oracle.gemm_w4a16(A, b, sfb, scale2, rows=rows)
     stats = check_close16(got[rows], ref, w.K, amax(A), wmax(b, sfb, scale2), what="w4a16 qkvz")
     assert stats["frac_exact"] > 0.9, stats
+
+
+def _random_shapes(seed, count):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 1200)), int(rng.integers(1, 200)) * 8, int(rng.integers(1, 10)) * 256)
+            for _ in range(count)]
+
+
+@pytest.mark.parametrize("M,N,K", _random_shapes(4242, 6))
+def test_w4a16_random_shapes_exact_integers(g, M, N, K):
+    # seeded ragged shapes; block scales 2^{-1..1}, integer activations and a
+    # power-of-two per-tensor scale keep every sum exact: bit-exact
+    rng = np.random.default_rng(M * 7 + N)
+    A = synth.bf16_small_ints((M, K), -3, 3, M + K)
+    b = synth.uniform_bytes(N * K // 2, N + K).reshape(N, K // 2)
+    sfb = rng.choice(np.array([0x30, 0x38, 0x40], dtype=np.uint8), size=(N, K // 16))
+    got = run(g, A, b, sfb, 0.5)
+    check_bitexact16(got, oracle.gemm_w4a16(A, b, sfb, 0.5), f"w4a16 random {M}x{N}x{K}")
