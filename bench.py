@@ -684,11 +684,21 @@ def measure_w4a16(torch, lib, synth, up, stream, dev, warmup, reps, check, bf16_
                                         sets[i][2].data_ptr(), scale2, cs[i].data_ptr(),
                                         w.M, w.N, w.K, sp))
     sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    # the two-pass form (weights converted into a workspace, then the dense GEMM)
+    import ctypes
+    ws_bytes = int(lib.gemm_w4a16_ws_workspace_bytes(w.N, w.K))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    fn2 = lambda i: check(lib.gemm_w4a16_ws(sets[i][0].data_ptr(), sets[i][1].data_ptr(),
+                                            sets[i][2].data_ptr(), scale2, cs[i].data_ptr(),
+                                            ws.data_ptr(), ctypes.c_size_t(ws_bytes),
+                                            w.M, w.N, w.K, sp))
+    sec2, _ = time_launches(torch, stream, fn2, n, warmup, reps)
     tf = 2.0 * w.M * w.N * w.K / sec / 1e12
-    del sets, cs
+    del sets, cs, ws
     return {"shape": name, "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
             "frac_bf16_peak": tf / bf16_peak,
-            "weight_bytes": int(b_h.size + sfb_h.size)}
+            "weight_bytes": int(b_h.size + sfb_h.size),
+            "two_pass_us": sec2 * 1e6}
 
 
 def measure_nvfp4_decode(torch, lib, synth, up, stream, dev, pk, warmup, reps, check, fp4_peak,

@@ -132,6 +132,31 @@ GB300GEMM_API int gemm_w4a16(const void* A, const void* b, const void* sfb, floa
                              int M, int N, int K, void* stream);
 
 /*
+ * gemm_w4a16_ws - gemm_w4a16 in two passes: the weights are first converted
+ * once into `workspace` (BF16 [N][K], w = e2m1 * e4m3, exact), then the
+ * dense CTA-pair GEMM multiplies A by them with the same tiles, K order and
+ * epilogue (bf16(scale2 * sum)).  Results are bit-identical to gemm_w4a16.
+ * For large M (prefill) this is faster: the fused kernel converts each
+ * weight tile once per 256-row block of A; at small M the fused kernel
+ * reads 3.6x fewer weight bytes and needs no workspace.
+ *
+ * Defined by: as gemm_w4a16.
+ *
+ *   A, b, sfb, scale2, C, M, N, K as for gemm_w4a16;  workspace: caller-owned
+ *   device memory of at least gemm_w4a16_ws_workspace_bytes(N, K) bytes,
+ *   16-byte aligned, not overlapping A, b, sfb or C; on return it holds the
+ *   converted weights.
+ * Errors: as gemm_w4a16; GEMM_ERR_NULL also for a NULL workspace,
+ * GEMM_ERR_SHAPE for one that is too small.
+ */
+GB300GEMM_API int gemm_w4a16_ws(const void* A, const void* b, const void* sfb, float scale2,
+                                void* C, void* workspace, size_t workspace_bytes, int M, int N,
+                                int K, void* stream);
+
+/* Workspace bytes gemm_w4a16_ws needs (N*K*2; 0 if N, K are invalid). */
+GB300GEMM_API size_t gemm_w4a16_ws_workspace_bytes(int N, int K);
+
+/*
  * gemm_bf16_nt_splitk - BF16 NT GEMM with the K dimension split into
  * `k_splits` chunks, for shapes with too few output tiles to fill the GPU:
  *     partial_s[m,n] = sum over the K blocks of split s of A[m,k] B[n,k]

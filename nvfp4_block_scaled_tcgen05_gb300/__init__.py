@@ -19,6 +19,8 @@ from .binding import (  # noqa: F401
     gemm_nvfp4_bs,
     gemm_selftest_wait_timeout,
     gemm_w4a16,
+    gemm_w4a16_ws,
+    gemm_w4a16_ws_workspace_bytes,
     library_path,
     load,
     status_string,

@@ -25,7 +25,7 @@ STATUS = {
     8: "GEMM_ERR_NO_DEVICE",
 }
 EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nn", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
-           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk", "gemm_w4a16",
+           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk", "gemm_w4a16", "gemm_w4a16_ws",
            "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
            "gemm_status_string")
 
@@ -63,6 +63,9 @@ def load() -> ctypes.CDLL:
             lib.gemm_bf16_nt_splitk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_bf16_nt_streamk.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, vp]
             lib.gemm_w4a16.argtypes = [vp, vp, vp, f, vp, i, i, i, vp]
+            lib.gemm_w4a16_ws.argtypes = [vp, vp, vp, f, vp, vp, ctypes.c_size_t, i, i, i, vp]
+            lib.gemm_w4a16_ws_workspace_bytes.argtypes = [i, i]
+            lib.gemm_w4a16_ws_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_bf16_nt_streamk_workspace_bytes.argtypes = []
             lib.gemm_bf16_nt_streamk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_nvfp4_bs_splitk.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
@@ -238,6 +241,36 @@ def gemm_w4a16(A: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor, scale2: floa
     _mat(C, torch.bfloat16, "C")
     _check(load().gemm_w4a16(A.data_ptr(), b.data_ptr(), sfb.data_ptr(), float(scale2),
                              C.data_ptr(), M, N, K, _stream_ptr(stream)), "gemm_w4a16")
+    return C
+
+
+def gemm_w4a16_ws_workspace_bytes(N: int, K: int) -> int:
+    return int(load().gemm_w4a16_ws_workspace_bytes(N, K))
+
+
+def gemm_w4a16_ws(A: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor, scale2: float,
+                  workspace: torch.Tensor | None = None, C: torch.Tensor | None = None,
+                  stream=None):
+    """gemm_w4a16 in two passes (weights converted once into the workspace)."""
+    _mat(A, torch.bfloat16, "A")
+    _mat(b, torch.uint8, "b")
+    _mat(sfb, torch.uint8, "sfb")
+    M, K = A.shape
+    N = b.shape[0]
+    if tuple(b.shape) != (N, K // 2) or tuple(sfb.shape) != (N, K // 16):
+        raise ValueError("shape mismatch")
+    if workspace is None:
+        workspace = torch.empty(max(gemm_w4a16_ws_workspace_bytes(N, K), 16), dtype=torch.uint8,
+                                device=A.device)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _mat(C, torch.bfloat16, "C")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().gemm_w4a16_ws(A.data_ptr(), b.data_ptr(), sfb.data_ptr(), float(scale2),
+                                C.data_ptr(), workspace.data_ptr(), nbytes, M, N, K,
+                                _stream_ptr(stream)), "gemm_w4a16_ws")
     return C
 
 

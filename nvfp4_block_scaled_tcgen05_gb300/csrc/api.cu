@@ -265,6 +265,37 @@ int gemm_w4a16(const void* A, const void* b, const void* sfb, float scale2, void
                            scale2, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
 }
 
+int gemm_w4a16_ws(const void* A, const void* b, const void* sfb, float scale2, void* C,
+                  void* workspace, size_t workspace_bytes, int M, int N, int K, void* stream) {
+  if (!A || !b || !sfb || !C || !workspace) return GEMM_ERR_NULL;
+  if (M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_SHAPE;
+  const long long tiles = (long long)((M + 255) / 256) * ((N + 255) / 256);
+  if (tiles > kMaxTiles) return GEMM_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(b) || !aligned16(sfb) || !aligned16(C) || !aligned16(workspace))
+    return GEMM_ERR_ALIGN;
+  if (K % 256 != 0 || N % 8 != 0) return GEMM_ERR_ALIGN;
+  const size_t need = size_t(N) * size_t(K) * 2;
+  if (workspace_bytes < need) return GEMM_ERR_SHAPE;
+  const size_t sa = size_t(M) * K * 2, sbq = size_t(N) * (K / 2), ss = size_t(N) * (K / 16);
+  const size_t sc = size_t(M) * N * 2;
+  if (overlaps(C, sc, A, sa) || overlaps(C, sc, b, sbq) || overlaps(C, sc, sfb, ss) ||
+      overlaps(workspace, need, A, sa) || overlaps(workspace, need, b, sbq) ||
+      overlaps(workspace, need, sfb, ss) || overlaps(workspace, need, C, sc))
+    return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != GEMM_OK) return rc;
+  return launch_gemm_w4a16_twopass(A, static_cast<const uint8_t*>(b),
+                                   static_cast<const uint8_t*>(sfb), scale2, C,
+                                   static_cast<uint16_t*>(workspace), M, N, K, dev,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+size_t gemm_w4a16_ws_workspace_bytes(int N, int K) {
+  if (N <= 0 || K <= 0 || K % 256 != 0) return 0;
+  return size_t(N) * size_t(K) * 2;
+}
+
 int gemm_bf16_nt_ordered(const void* A, const void* B, float* C, int M, int N, int K,
                          void* stream) {
   int rc = check_bf16_nt(A, B, C, M, N, K, 4);

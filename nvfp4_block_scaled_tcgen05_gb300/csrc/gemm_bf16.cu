@@ -331,6 +331,18 @@ int launch_gemm_bf16_splitk(const void* A, const void* B, void* C, float* ws, in
   return launch_splitk_reduce(ws, C, size_t(M) * N, s_eff, dev, stream);
 }
 
+// C = bf16(scale * A.B^T) on the plain-output pair configuration (the
+// epilogue of the W4A16 GEMM, whose tiles and K order it shares).
+int launch_gemm_bf16_scale(const void* A, const void* B, void* C, int M, int N, int K,
+                           float scale, const DeviceInfo& dev, cudaStream_t stream) {
+  using Cfg = Bf16PairStore;
+  CUtensorMap ta, tb, tc;
+  GemmParams p;
+  const int rc = setup_bf16<Cfg>(A, B, C, M, N, K, scale, dev, ta, tb, tc, p);
+  if (rc != GEMM_OK) return rc;
+  return launch_tcgen05<Cfg, Epilogue::kScaleBF16>(ta, tb, tc, ta, ta, p, dev, stream);
+}
+
 int launch_gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int K,
                         const DeviceInfo& dev, cudaStream_t stream) {
   int cg = (M > 128) ? 2 : 1;

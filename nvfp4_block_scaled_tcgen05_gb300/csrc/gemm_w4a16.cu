@@ -7,6 +7,8 @@
 // stage into exact BF16 in the stage; the MMAs are the BF16 kind::f16 MMAs of the
 // dense GEMM; the epilogue multiplies the FP32 sum by scale2 once.  The
 // weights are read once per tile from L2/HBM at 4.5 bits each instead of 16.
+#include <algorithm>
+
 #include "launch.cuh"
 
 namespace gb300 {
@@ -51,6 +53,50 @@ int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float
   p.timeout_ns = wait_timeout_ns();
   // the A-scale map is unused; pass A's map in its place
   return launch_tcgen05<Cfg, Epilogue::kScaleBF16>(ta, tcode, tc, ta, tscale, p, dev, stream);
+}
+
+}  // namespace gb300
+
+namespace gb300 {
+
+namespace {
+
+// Weight conversion for the two-pass form: w[n][k] = e2m1 * e4m3 (exact in
+// BF16), written row-major [N][K].  One thread per 32 weights (16 code
+// bytes, 2 scale bytes -> 64 output bytes); consecutive threads take
+// consecutive 32-weight chunks of a row.
+__global__ void __launch_bounds__(256)
+    w4a16_convert_kernel(const uint8_t* __restrict__ b, const uint8_t* __restrict__ sfb,
+                         uint16_t* __restrict__ w, size_t chunks, int K) {
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  const size_t per_row = size_t(K) / 32;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < chunks; i += stride) {
+    const size_t n = i / per_row, c = i - n * per_row;
+    const uint4 codes = __ldg(reinterpret_cast<const uint4*>(b) + i);
+    const uint16_t sc = __ldg(reinterpret_cast<const unsigned short*>(sfb + n * (K / 16)) + c);
+    uint32_t v[16];
+    w4_dequant32(codes, sc, v);
+    uint4* dst = reinterpret_cast<uint4*>(w + n * size_t(K) + c * 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  }
+}
+
+}  // namespace
+
+// Two-pass W4A16: convert the weights once into ws ([N][K] BF16), then the
+// dense CTA-pair GEMM with the same tiles, K order and epilogue as the
+// fused kernel (bit-identical results).  For large M the conversion is paid
+// once instead of once per M block.
+int launch_gemm_w4a16_twopass(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2,
+                              void* C, uint16_t* ws, int M, int N, int K, const DeviceInfo& dev,
+                              cudaStream_t stream) {
+  const size_t chunks = size_t(N) * size_t(K) / 32;
+  const size_t want = (chunks + 255) / 256;
+  const int grid = int(std::max<size_t>(1, std::min<size_t>(want, size_t(dev.num_sms) * 16)));
+  w4a16_convert_kernel<<<grid, 256, 0, stream>>>(b, sfb, ws, chunks, K);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  return launch_gemm_bf16_scale(A, ws, C, M, N, K, scale2, dev, stream);
 }
 
 }  // namespace gb300

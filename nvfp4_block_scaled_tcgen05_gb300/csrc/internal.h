@@ -89,6 +89,13 @@ int launch_gemm_bf16_streamk(const void* A, const void* B, void* C, float* ws, i
 // b [N][K/2] (low nibble = even k), sfb [N][K/16]; K % 256 == 0, N % 8 == 0.
 int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2, void* C,
                       int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+// Two-pass W4A16: weights converted into ws ([N][K] BF16), then the pair GEMM
+// with the scale2 epilogue (launch_gemm_bf16_scale).
+int launch_gemm_w4a16_twopass(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2,
+                              void* C, uint16_t* ws, int M, int N, int K, const DeviceInfo& dev,
+                              cudaStream_t stream);
+int launch_gemm_bf16_scale(const void* A, const void* B, void* C, int M, int N, int K,
+                           float scale, const DeviceInfo& dev, cudaStream_t stream);
 // C[i] = bf16(sum_{s=0..S-1} ws[s*n + i]) in split order (_f16: FP16).
 int launch_splitk_reduce(const float* ws, void* C, size_t n, int splits, const DeviceInfo& dev,
                          cudaStream_t stream);

@@ -214,3 +214,18 @@ def test_w4a16_rejects_bad_arguments(lib, args, expect):
     f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.c_void_p] + [ctypes.c_int] * 3 + \
         [ctypes.c_void_p]
     assert f(*args, None) == expect
+
+
+def test_w4a16_ws_workspace_and_arguments(lib):
+    ws = lib.gemm_w4a16_ws_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(12288, 2048) == 12288 * 2048 * 2
+    assert ws(8, 224) == 0 and ws(0, 256) == 0
+    f = lib.gemm_w4a16_ws
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_size_t] + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    big = 1 << 20
+    assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 0, big, 8, 8, 256, None) == 1           # NULL workspace
+    assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 5 * P + 8, big, 8, 8, 256, None) == 3   # misaligned
+    assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 5 * P, 16, 8, 8, 256, None) == 2        # too small
+    assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 4 * P + 16, big, 8, 8, 256, None) == 4  # on C

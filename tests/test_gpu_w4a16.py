@@ -141,3 +141,35 @@ def test_w4a16_random_shapes_exact_integers(g, M, N, K):
     sfb = rng.choice(np.array([0x30, 0x38, 0x40], dtype=np.uint8), size=(N, K // 16))
     got = run(g, A, b, sfb, 0.5)
     check_bitexact16(got, oracle.gemm_w4a16(A, b, sfb, 0.5), f"w4a16 random {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 768), (1, 8, 256), (1016, 12288, 2048),
+                                   (129, 264, 512)])
+def test_w4a16_two_pass_equals_fused(g, M, N, K):
+    # same tiles, K order and epilogue: bit-identical to the fused kernel,
+    # and the workspace holds the exact converted weights
+    w = synth.W4a16("t", M, N, K, 0.0123, 500 + M)
+    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+    Ad, bd, sd = to_dev_bf16(A), to_dev_u8(b), to_dev_u8(sfb)
+    ws = torch.empty(g.gemm_w4a16_ws_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    two = bits16(g.gemm_w4a16_ws(Ad, bd, sd, scale2, ws))
+    fused = bits16(g.gemm_w4a16(Ad, bd, sd, scale2))
+    check_bitexact16(two, fused, f"two-pass vs fused {M}x{N}x{K}")
+    if M <= 512:
+        check_close16(two, oracle.gemm_w4a16(A, b, sfb, scale2), K, amax(A),
+                      wmax(b, sfb, scale2), what="two-pass vs oracle")
+    # the converted weights: one-hot rows of A read them back through the oracle
+    W = ws.view(torch.int16).view(N, K).cpu().numpy().view(np.uint16)
+    eye = np.zeros((K, K), dtype=np.uint16)
+    eye[np.arange(K), np.arange(K)] = 0x3F80
+    ref = oracle.gemm_w4a16(eye, b[:8], sfb[:8], 1.0)       # [K][8]: weights of rows 0..7
+    check_bitexact16(W[:8].T.copy(), ref, "converted weights")
+
+
+def test_w4a16_two_pass_rejects_a_small_workspace(g):
+    A = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((256, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(g.GemmError):
+        g.gemm_w4a16_ws(A, b, s, 1.0, ws)
