@@ -13,8 +13,6 @@
 // old output of the next tile streams in while the current tile is written.
 // The MMA sequence of a tile does not depend on the stage count, so every
 // configuration with the same CTA group produces the same accumulators.
-#include <cstdlib>
-
 #include "launch.cuh"
 
 namespace gb300 {
@@ -22,12 +20,10 @@ namespace gb300 {
 using Bf16Pair = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;
 using Bf16Single = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2>;
 // plain BF16 output: 128-deep stages (8 MMAs per stage), 3 stages
-using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 1, 2>;
+using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 2>;
 // NN layout (B stored [K][N]): the same tiles with B staged MN-major
-using Bf16PairStoreNN = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 1, 2, true>;
-using Bf16SingleNN = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2, true, false, 1, 1, true>;
-// two pairs per cluster sharing (multicasting) their A rows
-using Bf16PairMC = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2, true, false, 2>;
+using Bf16PairStoreNN = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 2, true>;
+using Bf16SingleNN = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2, true, false, 1, true>;
 // scaled-acc with K <= 256 (the LoRA fold): bound by streaming the output;
 // 8 epilogue warps (each 128 of the 256 columns, 4 output buffers) keep more
 // of that stream in flight than 4 (measured 75.9 -> 68.9 us at 4096 x 17408)
@@ -42,7 +38,7 @@ static int setup_bf16(const void* A, const void* B, void* C, int M, int N, int K
                       const DeviceInfo& dev, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tc,
                       GemmParams& p) {
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
-                          64, Cfg::A_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+                          64, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == GEMM_OK) {
     if constexpr (Cfg::B_MN)  // B [K][N]: boxes of 64 columns x BK rows
       rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, uint64_t(N), uint64_t(K), 1,
@@ -63,7 +59,7 @@ static int setup_bf16(const void* A, const void* B, void* C, int M, int N, int K
   p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = (K + Cfg::BK - 1) / Cfg::BK;
-  p.total_tiles = p.num_m_blocks * ((p.num_n_blocks + Cfg::MC - 1) / Cfg::MC);
+  p.total_tiles = p.num_m_blocks * p.num_n_blocks;
   p.group_m = raster_group_m(p.num_m_blocks, (long long)Cfg::TILE_M * K * 2);
   p.k_splits = 1;
   p.kb_per_split = p.num_k_blocks;
@@ -173,7 +169,7 @@ static void build_streamk_plan(const GemmParams& p, int C, StreamKPlan& plan) {
     const int c1 = int((te * P + T - 1) / T - 1);
     if (c1 == c0) continue;
     int l, mb, nb;
-    decode_tile<Cfg>(dp_rounds * C + t, p, 0, l, mb, nb);
+    decode_tile<Cfg>(dp_rounds * C + t, p, l, mb, nb);
     const int i = plan.tiles++;
     plan.mb[i] = uint32_t(mb);
     plan.nb[i] = uint32_t(nb);
@@ -190,13 +186,10 @@ static void build_streamk_plan(const GemmParams& p, int C, StreamKPlan& plan) {
 // they save.  Among P = 1..C the host takes the P that minimises
 // ceil(T / P) K iterations on the critical path plus 0.1 iteration for each
 // partial tile written and summed (T / P + tail of them), the ratio measured
-// on the 5120 x 2048 x {2048, 11008} GEMMs.  GB300GEMM_SK_PAIRS=P (tests,
-// tuning) forces the division over min(P, C) clusters.
+// on the 5120 x 2048 x {2048, 11008} GEMMs.  A testing override
+// (gemm_testing_set_overrides) forces the division over min(P, C) clusters.
 static int streamk_share(int tiles, int kbt, int C) {
-  if (const char* e = std::getenv("GB300GEMM_SK_PAIRS")) {
-    const int v = std::atoi(e);
-    if (v >= 1) return v < C ? v : C;
-  }
+  if (const int v = streamk_clusters_override()) return v < C ? v : C;
   const int tail = tiles % C;
   if (tail == 0 || 4 * tail > C) return 0;
   const long long T = (long long)tail * kbt;
@@ -219,8 +212,8 @@ static int streamk_share(int tiles, int kbt, int C) {
 template <class Cfg>
 static int run_bf16_streamk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
                             const DeviceInfo& dev, cudaStream_t stream) {
-  static_assert(!Cfg::kRegEpi && Cfg::EPI_BUFS > 0 && Cfg::MC == 1,
-                "partial tiles are written by the TMA-store epilogue of single-pair clusters");
+  static_assert(!Cfg::kRegEpi && Cfg::EPI_BUFS > 0,
+                "partial tiles are written by the TMA-store epilogue");
   CUtensorMap ta, tb, tc, tw;
   GemmParams p;
   int rc = setup_bf16<Cfg>(A, B, C, M, N, K, 0.0f, dev, ta, tb, tc, p);
@@ -363,15 +356,8 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   // one CTA on 128 rows, so pairs (128-deep stages, half the B traffic per
   // SM) occupy as many SMs as single CTAs whenever M spans two row blocks.
   if (!scaled_acc && !cta_group_override()) cg = (M > 128) ? 2 : 1;
-  if (!scaled_acc && cg == 2) {
-    // GB300GEMM_MC=2 selects the A-multicast cluster; measured no faster
-    // than the plain pair on the shapes here (GB300), so it is opt-in.
-    const char* e = std::getenv("GB300GEMM_MC");
-    const bool mc = e && std::atoi(e) == 2;
-    if (mc && (N + 255) / 256 >= 2)
-      return run_bf16<Bf16PairMC>(A, B, C, M, N, K, 0.0f, false, dev, stream);
+  if (!scaled_acc && cg == 2)
     return run_bf16<Bf16PairStore>(A, B, C, M, N, K, 0.0f, false, dev, stream);
-  }
   return cg == 2 ? run_bf16<Bf16Pair>(A, B, C, M, N, K, scale, scaled_acc, dev, stream)
                  : run_bf16<Bf16Single>(A, B, C, M, N, K, scale, scaled_acc, dev, stream);
 }

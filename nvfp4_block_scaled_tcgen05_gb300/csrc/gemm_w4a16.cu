@@ -15,14 +15,14 @@ namespace gb300 {
 
 // direct-store epilogue (no output buffers): the shared memory holds the
 // code / scale ring instead
-using W4Pair = TileCfg<Operand::kW4A16, 2, 256, 3, 4, 0, true, false, 1, 2>;
+using W4Pair = TileCfg<Operand::kW4A16, 2, 256, 3, 4, 0, true, false, 2>;
 
 int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2, void* C,
                       int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   using Cfg = W4Pair;
   CUtensorMap ta, tcode, tscale, tc;
   int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
-                          64, Cfg::A_SLICE_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+                          64, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
   // codes: N rows of K/2 bytes, 64-byte x B_ROWS boxes (one K block of the
   // CTA's weight rows); scales: N rows of K/16 bytes, 16-byte boxes
   if (rc == GEMM_OK)

@@ -213,18 +213,6 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* 
       : "memory");
 }
 
-// Pair load multicast to the CTAs of `mask`: the box lands at the same
-// offset in each of them, and each one's pair leader is signalled on the
-// barrier at `bar`'s offset (`bar` addresses this CTA's pair leader).
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar,
-                                                    int x, int y, int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 // CG is the CTA group: 1 (one SM) or 2 (a CTA pair sharing each MMA).
 template <int CG>
@@ -266,9 +254,9 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // Arrive (once) on an mbarrier when every tcgen05 operation this thread
-// issued before has completed.  With CG == 2 the arrive is multicast to the
-// barrier at the same offset in every CTA of `mask` (cluster ranks; the
-// default is the pair of a two-CTA cluster).
+// issued before has completed.  With CG == 2 the arrive (an mbarrier
+// signal, not a data copy) goes to the barrier at the same offset in every
+// CTA of `mask` (cluster ranks; the default is both CTAs of the pair).
 template <int CG>
 __device__ __forceinline__ void tc_commit(uint32_t bar, uint16_t mask = 3) {
   if constexpr (CG == 1)

@@ -66,8 +66,7 @@ struct GemmParams {
 };
 
 template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
-          bool SFA_REP_ = true, bool SFB_REP_ = false, int MC_ = 1, int KSUB_ = 1,
-          bool B_MN_ = false>
+          bool SFA_REP_ = true, bool SFB_REP_ = false, int KSUB_ = 1, bool B_MN_ = false>
 struct TileCfg {
   static constexpr Operand kOp = OP;
   static constexpr bool kFP4 = (OP == Operand::kNVFP4);
@@ -75,12 +74,7 @@ struct TileCfg {
   // stage by dedicated warps instead of being loaded by TMA.
   static constexpr bool kW4 = (OP == Operand::kW4A16);
   static constexpr int CG = CG_;                  // CTAs per MMA (1 or 2)
-  // MC = 2: a cluster of two CTA pairs computes two horizontally adjacent
-  // tiles that share their A rows.  Each CTA loads half of its 128 A rows
-  // and multicasts them to the CTA with the same role in the other pair, so
-  // the L2 serves every A byte once per cluster instead of once per pair.
-  static constexpr int MC = MC_;
-  static constexpr int CLUSTER = CG * MC;         // CTAs per cluster
+  static constexpr int CLUSTER = CG;              // CTAs per cluster: the MMA's CTA group
   static constexpr int BM = 128;                  // A rows / TMEM lanes per CTA
   static constexpr int TILE_M = BM * CG;          // C rows per tile
   static constexpr int BN = BN_;                  // C columns per tile (MMA N)
@@ -138,12 +132,9 @@ struct TileCfg {
   static_assert(NUM_ACC * BN + STAGES * SF_COLS <= TMEM_COLS, "TMEM column budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(CG == 1 || CG == 2, "CTA group");
-  static_assert(MC == 1 || (MC == 2 && CG == 2 && !kFP4), "A multicast: BF16 CTA pairs only");
   static_assert(KSUB == 1 || (KSUB == 2 && !kFP4), "K sub-tiles: BF16 only");
-  static_assert(!B_MN || (!kFP4 && MC_ == 1 && B_ROWS % 64 == 0), "MN-major B: BF16, no multicast");
+  static_assert(!B_MN || (!kFP4 && B_ROWS % 64 == 0), "MN-major B: BF16 operands");
   static constexpr int B_ATOM_BYTES = 64 * KSUB * 128;  // one 64-column MN-major atom of a stage
-  static constexpr int A_SLICE_ROWS = BM / MC;    // A rows each CTA loads per stage
-  static constexpr int A_SLICE_BYTES = A_SLICE_ROWS * 128;
   // the MMA issuer releases a stage only after the next stage's first MMA
   static_assert(STAGES >= 2, "at least two pipeline stages");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA");
@@ -170,8 +161,8 @@ struct TileCfg {
   static constexpr int RAW_CODE_BYTES = kW4 ? B_ROWS * 64 : 0;  // codes of a job
   static constexpr int RAW_BYTES = kW4 ? B_ROWS * (64 + 16) : 0;  // + the scale pairs
   static constexpr int RAW_RING_BYTES = RAW_STAGES * RAW_BYTES;
-  static_assert(!kW4 || (KSUB == 2 && MC == 1 && !B_MN && DQ_ROWS % 8 == 0 && B_ROWS <= 256),
-                "W4A16: 128-deep stages, no multicast, K-major B");
+  static_assert(!kW4 || (KSUB == 2 && !B_MN && DQ_ROWS % 8 == 0 && B_ROWS <= 256),
+                "W4A16: 128-deep stages, K-major B");
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], epi[W][B], mma_done,
   // sf_full[S] (NVFP4) or bq_full[S], raw_full[R], raw_empty[R] (W4A16)
   static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1 +
@@ -198,24 +189,21 @@ struct TileCfg {
   }
 };
 
-// Cluster work item `tile` -> batch l, M block mb and this pair's N block
-// nb.  With MC pairs per cluster an item spans MC adjacent N blocks and pair
-// `pair` takes the pair-th (which may lie past N: the pair then still loads
-// and multiplies, for its partner's sake, but stores nothing).
+// Work item `tile` -> batch l, M block mb and N block nb, in grouped-M
+// raster order: consecutive items walk group_m M blocks down one N column.
 template <class Cfg>
-__host__ __device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int pair,
-                                                     int& l, int& mb, int& nb) {
-  const int n_items = (p.num_n_blocks + Cfg::MC - 1) / Cfg::MC;
-  const int per_batch = p.num_m_blocks * n_items;
+__host__ __device__ __forceinline__ void decode_tile(int tile, const GemmParams& p, int& l,
+                                                     int& mb, int& nb) {
+  const int per_batch = p.num_m_blocks * p.num_n_blocks;
   l = tile / per_batch;
   const int t = tile - l * per_batch;
-  const int group_tiles = p.group_m * n_items;
+  const int group_tiles = p.group_m * p.num_n_blocks;
   const int g = t / group_tiles;
   const int first_m = g * p.group_m;
   const int gm = (p.num_m_blocks - first_m < p.group_m) ? p.num_m_blocks - first_m : p.group_m;
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
-  nb = (r / gm) * Cfg::MC + pair;
+  nb = r / gm;
 }
 
 // One work segment of a cluster: K blocks [kb0, kb1) of tile `tile`; slot
@@ -245,7 +233,7 @@ __device__ __forceinline__ bool seg_at(const GemmParams& p, int c, int C, int id
     s.kb1 = p.num_k_blocks;
     if (p.k_splits > 1) {
       int l, mb, nb;
-      decode_tile<Cfg>(s.tile, p, 0, l, mb, nb);
+      decode_tile<Cfg>(s.tile, p, l, mb, nb);
       s.kb0 = l * p.kb_per_split;
       s.kb1 = min(p.num_k_blocks, s.kb0 + p.kb_per_split);
     }
@@ -470,23 +458,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int MC = Cfg::MC;
   const uint32_t rank = (Cfg::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;
   const uint32_t peer = (CG == 2) ? (rank & 1u) : 0u;  // role within the CTA pair
-  const int pair = int(rank) / CG;                     // pair index within the cluster
-  const uint32_t pair_leader = rank & ~1u;             // rank of this pair's MMA issuer
+  const uint32_t pair_leader = 0u;                     // rank of the pair's MMA issuer
   const bool leader = (peer == 0);
   const int cluster_id = blockIdx.x / Cfg::CLUSTER;
   const int num_clusters = gridDim.x / Cfg::CLUSTER;
-  // tcgen05.commit targets: this pair's two CTAs; stage releases go to every
-  // CTA whose producer writes into this pair's shared memory (all of them)
-  const uint16_t pair_mask = uint16_t(3u << pair_leader);
-  const uint16_t release_mask = (MC == 2) ? uint16_t(0xF) : pair_mask;
+  // tcgen05.commit targets: both CTAs of the pair (stage releases and
+  // accumulator hand-over)
+  const uint16_t pair_mask = uint16_t(3u);
+  const uint16_t release_mask = pair_mask;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), MC);  // one release per pair reading the stage
+      ptx::mbar_init(empty_bar(s), 1);  // released by the MMA issuer's commit
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(acc_full(b), 1);
@@ -584,7 +570,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       Seg sg;
       for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
         int l, mb, nb;
-        decode_tile<Cfg>(sg.tile, p, pair, l, mb, nb);
+        decode_tile<Cfg>(sg.tile, p, l, mb, nb);
         const int a_row = mb * Cfg::TILE_M + int(peer) * Cfg::BM;
         const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
         int sfb_atoms = 0;
@@ -653,13 +639,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
               const uint32_t da = stage_a(stage) + sub * Cfg::A_SUB_BYTES;
               const uint32_t db = stage_b(stage) + sub * Cfg::B_SUB_BYTES;
-              if constexpr (MC == 2) {
-                // this CTA's half of the shared A rows, to both pairs
-                const uint16_t a_mask = uint16_t((1u << peer) | (1u << (2 + peer)));
-                ptx::tma_load_3d_pair_mc(da + pair * Cfg::A_SLICE_BYTES, &tmap_a, fb, x,
-                                         a_row + pair * Cfg::A_SLICE_ROWS, l, a_mask);
-                ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
-              } else if constexpr (Cfg::B_MN) {
+              if constexpr (Cfg::B_MN) {
                 ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 if (sub == 0)
 #pragma unroll
@@ -729,7 +709,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       Seg sg;
       for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
         int l, mb, nb;
-        decode_tile<Cfg>(sg.tile, p, pair, l, mb, nb);
+        decode_tile<Cfg>(sg.tile, p, l, mb, nb);
         const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!wait_bar(raw_empty(q), qphase ^ 1u, w, 10)) {
@@ -1054,7 +1034,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if constexpr (kLookahead) {
         constexpr int NCH = Cfg::EPI_COLS / 64;
         int l2, mb2, nb2;
-        decode_tile<Cfg>(s2.tile, p, pair, l2, mb2, nb2);
+        decode_tile<Cfg>(s2.tile, p, l2, mb2, nb2);
         const int r0 = mb2 * Cfg::TILE_M + int(peer) * Cfg::BM + q * 32;
         if (r0 >= p.M) return;
 #pragma unroll
@@ -1076,7 +1056,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx, ++it) {
       int l, mb, nb;
-      decode_tile<Cfg>(sg.tile, p, pair, l, mb, nb);
+      decode_tile<Cfg>(sg.tile, p, l, mb, nb);
       const int acc = it % Cfg::NUM_ACC;
       const uint32_t acc_phase = uint32_t(it / Cfg::NUM_ACC) & 1u;
       if constexpr (kLookahead) {

@@ -25,14 +25,12 @@ def g():
     assert lib.gemm_get_device_status() == 0
 
 
-@pytest.fixture(params=[(1, 1), (2, 1), (2, 2)], ids=["cta1", "cta2", "cta2x2"])
-def cg(request, monkeypatch):
-    """Force the single-CTA kernel, the CTA-pair (cta_group::2) kernel, or
-    two CTA pairs per cluster sharing their A rows by TMA multicast."""
-    group, mc = request.param
-    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(group))
-    monkeypatch.setenv("GB300GEMM_MC", str(mc))
-    return group
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
+def cg(request, g):
+    """Force the single-CTA kernel or the CTA-pair (cta_group::2) kernel."""
+    g.gemm_testing_set_overrides(cta_group=request.param)
+    yield request.param
+    g.gemm_testing_set_overrides()
 
 
 def amax(x):
