@@ -12,7 +12,13 @@
  *    return a GEMM_ERR_* code without side effects when validation fails;
  *  - return GEMM_OK (0) when the work was enqueued.
  *
- * Device-side wait limits: every wait inside a kernel is bounded (about two
+ * One-time set-up: the first call of any entry point on a device (with that
+ * device current) reads its attributes and looks up the device addresses of
+ * the library's own __device__ variables.  Make that first call outside any
+ * stream capture; during a capture it returns GEMM_ERR_CAPTURE and does
+ * nothing (a later call outside capture does the set-up).
+ *
+ * Device-side wait limits: every wait inside a kernel is bounded (two
  * seconds).  A kernel that runs out of a wait stops, records a code in a
  * device status word and returns; gemm_get_device_status() reports it.
  *
@@ -44,6 +50,7 @@ extern "C" {
 #define GEMM_ERR_LAUNCH     6  /* a CUDA call failed (launch, attribute, tensor-map encode) */
 #define GEMM_ERR_TIMEOUT    7  /* a kernel ran out of a bounded device-side wait */
 #define GEMM_ERR_NO_DEVICE  8  /* no usable CUDA device / driver */
+#define GEMM_ERR_CAPTURE    9  /* the first call on a device was made during stream capture */
 
 /*
  * gemm_bf16_nt - dense BF16 GEMM, C = bf16(A . B^T) with FP32 accumulation.
@@ -234,16 +241,18 @@ GB300GEMM_API size_t gemm_bf16_nt_streamk_workspace_bytes(void);
  *   Limit: S * M * N * 4 <= GEMM_SPLITK_STATIC_SCRATCH_BYTES, with S the
  *   splits actually used (gemm_bf16_nt_splitk_workspace_bytes); larger
  *   problems are rejected with GEMM_ERR_SHAPE before anything is launched.
- *   The first call on each device looks up the scratch array's device
- *   address (cudaGetSymbolAddress with that device current); make that first
- *   call before any stream capture.
+ *   The scratch array's device address is looked up (cudaGetSymbolAddress
+ *   with that device current) in the library's one-time per-device set-up,
+ *   i.e. by the first call of any entry point on the device; make that first
+ *   call before any stream capture (during a capture it returns
+ *   GEMM_ERR_CAPTURE).
  *   All calls share the one array and it keeps the last call's contents; no
  *   element needs to start at zero (each call writes every element it reads
  *   before reading it).  Calls whose executions overlap on the GPU (other
  *   streams, other host threads) race on the array and give wrong results:
  *   order them on one stream or with events.
  * Errors: GEMM_ERR_NULL, _SHAPE (dims, k_splits, or over the limit),
- * _ALIGN, _ALIAS, _ARCH, _NO_DEVICE, _LAUNCH.
+ * _ALIGN, _ALIAS, _ARCH, _NO_DEVICE, _CAPTURE, _LAUNCH.
  */
 #define GEMM_SPLITK_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 GB300GEMM_API int gemm_bf16_nt_splitk_static(const void* A, const void* B, void* C, int M, int N,
@@ -366,6 +375,22 @@ GB300GEMM_API int gemm_get_device_status(void* stream);
  * Errors: GEMM_ERR_SHAPE (timeout out of range), _ARCH, _NO_DEVICE, _LAUNCH.
  */
 GB300GEMM_API int gemm_selftest_wait_timeout(int timeout_ms, void* stream);
+
+/*
+ * gemm_testing_set_overrides - process-wide testing hook, not for production
+ * use.  Forces choices the library otherwise makes from the shape, so that
+ * tests can reach every kernel configuration:
+ *   cta_group         0 = by shape; 1 or 2 = the single-CTA or the CTA-pair
+ *                     configuration of gemm_bf16_nt, gemm_bf16_nn,
+ *                     gemm_bf16_nt_scaled_acc and the BF16 split-K calls;
+ *   streamk_clusters  0 = by shape; P >= 1 = gemm_bf16_nt_streamk divides the
+ *                     last round's K iterations over min(P, pairs) CTA pairs.
+ * Results stay within each call's documented accuracy whatever is forced.
+ * Takes effect for calls made after it returns.  Library extension (the
+ * pages define no such call).
+ * Errors: GEMM_ERR_SHAPE (a value out of range).
+ */
+GB300GEMM_API int gemm_testing_set_overrides(int cta_group, int streamk_clusters);
 
 /* gemm_status_string - static, human-readable name of a status code. */
 GB300GEMM_API const char* gemm_status_string(int status);

@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     gemm_get_device_status,
     gemm_nvfp4_bs,
     gemm_selftest_wait_timeout,
+    gemm_testing_set_overrides,
     gemm_w4a16,
     gemm_w4a16_ws,
     gemm_w4a16_ws_workspace_bytes,

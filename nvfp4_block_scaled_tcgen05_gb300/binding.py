@@ -22,12 +22,12 @@ _lib = None
 STATUS = {
     0: "GEMM_OK", 1: "GEMM_ERR_NULL", 2: "GEMM_ERR_SHAPE", 3: "GEMM_ERR_ALIGN",
     4: "GEMM_ERR_ALIAS", 5: "GEMM_ERR_ARCH", 6: "GEMM_ERR_LAUNCH", 7: "GEMM_ERR_TIMEOUT",
-    8: "GEMM_ERR_NO_DEVICE",
+    8: "GEMM_ERR_NO_DEVICE", 9: "GEMM_ERR_CAPTURE",
 }
 EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nn", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
            "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk", "gemm_w4a16", "gemm_w4a16_ws",
            "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
-           "gemm_status_string")
+           "gemm_testing_set_overrides", "gemm_status_string")
 
 
 class GemmError(RuntimeError):
@@ -74,6 +74,7 @@ def load() -> ctypes.CDLL:
             lib.gemm_nvfp4_bs_splitk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_get_device_status.argtypes = [vp]
             lib.gemm_selftest_wait_timeout.argtypes = [i, vp]
+            lib.gemm_testing_set_overrides.argtypes = [i, i]
             lib.gemm_status_string.argtypes = [i]
             lib.gemm_status_string.restype = ctypes.c_char_p
             for name in EXPORTS[:-1]:
@@ -358,6 +359,13 @@ def gemm_selftest_wait_timeout(timeout_ms: int = 50, stream=None) -> None:
     """Launch the failure-path self test (a wait that must run out)."""
     _check(load().gemm_selftest_wait_timeout(int(timeout_ms), _stream_ptr(stream)),
            "gemm_selftest_wait_timeout")
+
+
+def gemm_testing_set_overrides(cta_group: int = 0, streamk_clusters: int = 0) -> None:
+    """Testing hook: force the CTA group of the BF16 launchers (1 or 2) and the
+    CTA pairs sharing a stream-K tail; 0 restores the shape's own choice."""
+    _check(load().gemm_testing_set_overrides(int(cta_group), int(streamk_clusters)),
+           "gemm_testing_set_overrides")
 
 
 def gemm_get_device_status(stream=None) -> int:

@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -60,7 +60,7 @@ constexpr long long kMaxTiles = 1ll << 30;
 
 }  // namespace
 
-int current_device(DeviceInfo* out) {
+int current_device(DeviceInfo* out, void* stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -69,39 +69,53 @@ int current_device(DeviceInfo* out) {
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceSlot& s = g_devices[dev];
   if (!s.ready) {
+    // One-time set-up of this device: attributes and the device addresses of
+    // the library's __device__ variables.  Symbol lookups may load the
+    // module, which a stream capture does not allow: refuse during capture
+    // and leave the set-up for a later call.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess ||
+        cap != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return GEMM_ERR_CAPTURE;
+    }
     DeviceInfo d{};
     d.device = dev;
-    int rc = GEMM_OK;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
             cudaSuccess ||
         cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
             cudaSuccess) {
-      rc = GEMM_ERR_NO_DEVICE;
-    } else if (!(d.cc_major == 10 && d.cc_minor == 3)) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_DEVICE;  // not cached: a later call retries
+    }
+    int rc = GEMM_OK;
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) {
       rc = GEMM_ERR_ARCH;  // the library carries sm_103a code only
     } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word) !=
-               cudaSuccess) {
-      rc = GEMM_ERR_NO_DEVICE;
+                   cudaSuccess ||
+               splitk_static_scratch_lookup(&d.splitk_scratch) != GEMM_OK) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_DEVICE;  // not cached: a later call retries
     }
-    if (rc != GEMM_OK) cudaGetLastError();
     s.info = d;
-    s.rc = rc;
+    s.rc = rc;  // GEMM_OK, or the permanent GEMM_ERR_ARCH
     s.ready = true;
   }
   *out = s.info;
   return s.rc;
 }
 
-unsigned long long wait_timeout_ns() {
-  static unsigned long long ns = [] {
-    const char* e = std::getenv("GB300GEMM_WAIT_TIMEOUT_MS");
-    long ms = e ? std::strtol(e, nullptr, 10) : 0;
-    if (ms <= 0) ms = 2000;
-    return static_cast<unsigned long long>(ms) * 1000000ull;
-  }();
-  return ns;
-}
+unsigned long long wait_timeout_ns() { return 2000ull * 1000000ull; }
+
+namespace {
+// Testing overrides (gemm_testing_set_overrides); 0 = the shape decides.
+std::atomic<int> g_test_cta_group{0};
+std::atomic<int> g_test_streamk_clusters{0};
+}  // namespace
+
+int testing_cta_group() { return g_test_cta_group.load(std::memory_order_relaxed); }
+int testing_streamk_clusters() { return g_test_streamk_clusters.load(std::memory_order_relaxed); }
 
 int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
                    uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
@@ -162,7 +176,7 @@ int gemm_bf16_nt(const void* A, const void* B, void* C, int M, int N, int K, voi
   if (rc != GEMM_OK) return rc;
   if (N % 8 != 0) return GEMM_ERR_ALIGN;  // 16-byte row pitch of C
   DeviceInfo dev;
-  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  if ((rc = current_device(&dev, stream)) != GEMM_OK) return rc;
   return launch_gemm_bf16(A, B, C, M, N, K, 0.0f, false, dev, static_cast<cudaStream_t>(stream));
 }
 
@@ -176,7 +190,7 @@ int gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int K, voi
   const size_t sa = size_t(M) * K * 2, sb = size_t(K) * N * 2, sc = size_t(M) * N * 2;
   if (overlaps(C, sc, A, sa) || overlaps(C, sc, B, sb)) return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_gemm_bf16_nn(A, B, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
 }
@@ -187,7 +201,7 @@ int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_inout, int M, 
   if (rc != GEMM_OK) return rc;
   if (N % 8 != 0) return GEMM_ERR_ALIGN;
   DeviceInfo dev;
-  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  if ((rc = current_device(&dev, stream)) != GEMM_OK) return rc;
   return launch_gemm_bf16(A, B, C_inout, M, N, K, scale, true, dev,
                           static_cast<cudaStream_t>(stream));
 }
@@ -209,7 +223,7 @@ int gemm_bf16_nt_splitk(const void* A, const void* B, void* C, void* workspace,
       overlaps(workspace, need, C, sc))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  if ((rc = current_device(&dev, stream)) != GEMM_OK) return rc;
   return launch_gemm_bf16_splitk(A, B, C, static_cast<float*>(workspace), M, N, K, k_splits, dev,
                                  static_cast<cudaStream_t>(stream));
 }
@@ -234,7 +248,7 @@ int gemm_bf16_nt_streamk(const void* A, const void* B, void* C, void* workspace,
       overlaps(workspace, workspace_bytes, C, sc))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  if ((rc = current_device(&dev, stream)) != GEMM_OK) return rc;
   if (workspace_bytes < streamk_workspace_bytes(dev)) return GEMM_ERR_SHAPE;
   return launch_gemm_bf16_streamk(A, B, C, static_cast<float*>(workspace), M, N, K, dev,
                                   static_cast<cudaStream_t>(stream));
@@ -242,7 +256,7 @@ int gemm_bf16_nt_streamk(const void* A, const void* B, void* C, void* workspace,
 
 size_t gemm_bf16_nt_streamk_workspace_bytes(void) {
   DeviceInfo dev;
-  if (current_device(&dev) != GEMM_OK) return 0;
+  if (current_device(&dev, nullptr) != GEMM_OK) return 0;
   return streamk_workspace_bytes(dev);
 }
 
@@ -259,7 +273,7 @@ int gemm_w4a16(const void* A, const void* b, const void* sfb, float scale2, void
   if (overlaps(C, sc, A, sa) || overlaps(C, sc, b, sbq) || overlaps(C, sc, sfb, ss))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_gemm_w4a16(A, static_cast<const uint8_t*>(b), static_cast<const uint8_t*>(sfb),
                            scale2, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
@@ -283,7 +297,7 @@ int gemm_w4a16_ws(const void* A, const void* b, const void* sfb, float scale2, v
       overlaps(workspace, need, sfb, ss) || overlaps(workspace, need, C, sc))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_gemm_w4a16_twopass(A, static_cast<const uint8_t*>(b),
                                    static_cast<const uint8_t*>(sfb), scale2, C,
@@ -301,7 +315,7 @@ int gemm_bf16_nt_ordered(const void* A, const void* B, float* C, int M, int N, i
   int rc = check_bf16_nt(A, B, C, M, N, K, 4);
   if (rc != GEMM_OK) return rc;
   DeviceInfo dev;
-  if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+  if ((rc = current_device(&dev, stream)) != GEMM_OK) return rc;
   return launch_gemm_router(A, B, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
 }
 
@@ -321,7 +335,7 @@ int gemm_nvfp4_bs(const void* a, const void* b, const void* sfa, const void* sfb
       overlaps(c, sc, sfb, ssb))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_gemm_nvfp4(a, b, sfa, sfb, c, L, M, N, K, dev, static_cast<cudaStream_t>(stream));
 }
@@ -360,7 +374,7 @@ int gemm_nvfp4_bs_splitk(const void* a, const void* b, const void* sfa, const vo
       overlaps(workspace, need, c, sc))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_gemm_nvfp4_splitk(a, b, sfa, sfb, c, static_cast<float*>(workspace), M, N, K,
                                   k_splits, dev, static_cast<cudaStream_t>(stream));
@@ -372,14 +386,14 @@ int bf16_scaled_add(void* out, const void* d, float scale, long n, void* stream)
   if (!aligned16(out) || !aligned16(d)) return GEMM_ERR_ALIGN;
   if (overlaps(out, size_t(n) * 2, d, size_t(n) * 2)) return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_scaled_add(out, d, scale, n, dev, static_cast<cudaStream_t>(stream));
 }
 
 int gemm_get_device_status(void* stream) {
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
@@ -396,10 +410,18 @@ int gemm_get_device_status(void* stream) {
   return GEMM_OK;
 }
 
+int gemm_testing_set_overrides(int cta_group, int streamk_clusters) {
+  if (cta_group != 0 && cta_group != 1 && cta_group != 2) return GEMM_ERR_SHAPE;
+  if (streamk_clusters < 0) return GEMM_ERR_SHAPE;
+  g_test_cta_group.store(cta_group, std::memory_order_relaxed);
+  g_test_streamk_clusters.store(streamk_clusters, std::memory_order_relaxed);
+  return GEMM_OK;
+}
+
 int gemm_selftest_wait_timeout(int timeout_ms, void* stream) {
   if (timeout_ms < 1 || timeout_ms > 10000) return GEMM_ERR_SHAPE;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_selftest_timeout(timeout_ms, dev, static_cast<cudaStream_t>(stream));
 }
@@ -415,6 +437,8 @@ const char* gemm_status_string(int status) {
     case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: a CUDA call failed";
     case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel ran out of a bounded wait";
     case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no usable CUDA device";
+    case GEMM_ERR_CAPTURE:
+      return "GEMM_ERR_CAPTURE: first call on this device made during stream capture";
     default: return "unknown status";
   }
 }

@@ -15,16 +15,29 @@ struct DeviceInfo {
   int device;
   int num_sms;
   int cc_major, cc_minor;
-  unsigned int* status;  // device address of the status word
+  unsigned int* status;   // device address of the status word
+  float* splitk_scratch;  // device address of the allocation-free split-K scratch
 };
 
-// Fills `out` for the current device.  Returns GEMM_OK, GEMM_ERR_NO_DEVICE
-// or GEMM_ERR_ARCH (not an sm_103 GPU).
-int current_device(DeviceInfo* out);
+// Fills `out` for the current device; the first call per device does the
+// one-time set-up (attributes, device addresses of the library's __device__
+// variables), which cannot run while `stream` is being captured.  Returns
+// GEMM_OK, GEMM_ERR_NO_DEVICE, GEMM_ERR_ARCH (not an sm_103 GPU) or
+// GEMM_ERR_CAPTURE (set-up still due and `stream` is capturing).
+int current_device(DeviceInfo* out, void* stream);
 
-// Bound on every device-side wait, in nanoseconds (default 2 s; the
-// environment variable GB300GEMM_WAIT_TIMEOUT_MS overrides it).
+// Device address of the allocation-free split-K scratch array on the
+// current device (splitk_static.cu); called by the per-device set-up.
+// Returns GEMM_OK or GEMM_ERR_NO_DEVICE.
+int splitk_static_scratch_lookup(float** out);
+
+// Bound on every device-side wait, in nanoseconds (2 s).
 unsigned long long wait_timeout_ns();
+
+// Testing overrides set by gemm_testing_set_overrides (0 = not set): the
+// CTA group of the BF16 launchers, and the clusters sharing a stream-K tail.
+int testing_cta_group();
+int testing_streamk_clusters();
 
 // Encodes a rank-3 tiled TMA descriptor for a dense row-major tensor
 // [d2][d1][d0] of `elem_bytes`-byte elements starting at `base`, with box

@@ -1,25 +1,19 @@
 // Host-side launch of tcgen05_gemm_kernel instantiations: one-time per-device
 // attributes, co-resident cluster count, cudaLaunchKernelEx with the cluster
-// dimension of the configuration (CTA group x pairs sharing A).
+// dimension of the configuration (its CTA group).
 #pragma once
 
 #include <algorithm>
 #include <atomic>
-#include <cstdlib>
 
 #include "internal.h"
 #include "tcgen05_gemm.cuh"
 
 namespace gb300 {
 
-// CTA-group override for tests and experiments: GB300GEMM_CTA_GROUP=1 or 2
-// forces that path when the shape allows it; anything else lets the shape decide.
-inline int cta_group_override() {
-  const char* e = std::getenv("GB300GEMM_CTA_GROUP");
-  if (!e) return 0;
-  const int v = std::atoi(e);
-  return (v == 1 || v == 2) ? v : 0;
-}
+// Testing overrides (gemm_testing_set_overrides): 0 lets the shape decide.
+inline int cta_group_override() { return testing_cta_group(); }
+inline int streamk_clusters_override() { return testing_streamk_clusters(); }
 
 template <class Cfg, Epilogue EPI>
 void fill_launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cudaStream_t stream) {

@@ -12,10 +12,11 @@
 // The array is a file-scope __device__ variable.  In host code its name only
 // stands in for the symbol (it is not a device address), so the address is
 // looked up once per device with cudaGetSymbolAddress, with that device
-// current, and that pointer is what the kernels receive.  Every GPU that
-// loads the library holds the array until the process exits.
+// current, during the library's per-device set-up (the first call of any
+// entry point on that device), and that pointer is what the kernels
+// receive.  Every GPU that loads the library holds the array until the
+// process exits.
 #include <cstdint>
-#include <mutex>
 
 #include "internal.h"
 
@@ -24,27 +25,19 @@ static __device__ __align__(256) float g_splitk_scratch[GEMM_SPLITK_STATIC_SCRAT
 
 namespace gb300 {
 
-namespace {
-
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-float* g_scratch_ptr[kMaxDevices];  // device address of g_splitk_scratch per device
-
-// Device address of the scratch array on the current device (looked up on
-// the first call per device).  Returns GEMM_OK or GEMM_ERR_NO_DEVICE.
-int scratch_address(int device, float** out) {
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[device]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_splitk_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return GEMM_ERR_NO_DEVICE;
-    }
-    g_scratch_ptr[device] = static_cast<float*>(p);
+// Called once per device, with that device current, by the library's
+// per-device set-up (current_device): the scratch array's device address.
+int splitk_static_scratch_lookup(float** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_splitk_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
   }
-  *out = g_scratch_ptr[device];
+  *out = static_cast<float*>(p);
   return GEMM_OK;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -72,12 +65,10 @@ extern "C" int gemm_bf16_nt_splitk_static(const void* A, const void* B, void* C,
   if (overlaps(C, sc, A, size_t(M) * K * 2) || overlaps(C, sc, B, size_t(N) * K * 2))
     return GEMM_ERR_ALIAS;
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  const int rc = current_device(&dev, stream);  // set-up looks up dev.splitk_scratch
   if (rc != GEMM_OK) return rc;
-  float* scratch = nullptr;
-  if ((rc = scratch_address(dev.device, &scratch)) != GEMM_OK) return rc;
   // Every element of the scratch that the reduce reads is written earlier in
   // this same call, so nothing needs clearing between calls.
-  return launch_gemm_bf16_splitk(A, B, C, scratch, M, N, K, k_splits, dev,
+  return launch_gemm_bf16_splitk(A, B, C, dev.splitk_scratch, M, N, K, k_splits, dev,
                                  static_cast<cudaStream_t>(stream));
 }

@@ -26,10 +26,11 @@ def g():
 
 
 @pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
-def cg(request, monkeypatch):
+def cg(request, g):
     """Force the single-CTA or the CTA-pair kernel."""
-    monkeypatch.setenv("GB300GEMM_CTA_GROUP", str(request.param))
-    return request.param
+    g.gemm_testing_set_overrides(cta_group=request.param)
+    yield request.param
+    g.gemm_testing_set_overrides()
 
 
 def amax(x):

@@ -28,12 +28,13 @@ def g():
 
 
 @pytest.fixture(params=["all", "5"], ids=["share_all", "share_5"])
-def share(request, monkeypatch):
+def share(request, g):
     """Force the stream-K division of the tail over every CTA pair, or over
     five pairs (several segments per pair); by default the library divides
     the tail only when it leaves most pairs idle."""
-    monkeypatch.setenv("GB300GEMM_SK_PAIRS", "4096" if request.param == "all" else "5")
-    return request.param
+    g.gemm_testing_set_overrides(streamk_clusters=4096 if request.param == "all" else 5)
+    yield request.param
+    g.gemm_testing_set_overrides()
 
 
 @pytest.fixture(scope="module")
@@ -74,10 +75,10 @@ def test_streamk_exact_integers_bitexact(g, ws, share, M, N, K):
     check_bitexact16(bits16(C), oracle.gemm_bf16_nt(A, B), f"stream-K exact {M}x{N}x{K}")
 
 
-def test_streamk_whole_tiles_equal_data_parallel(g, ws, monkeypatch):
+def test_streamk_whole_tiles_equal_data_parallel(g, ws):
     # qkv shape: 160 tiles, a tail of 8 on 76 pairs, which the default
     # schedule divides; all but the tail round are whole-tile work
-    monkeypatch.delenv("GB300GEMM_SK_PAIRS", raising=False)
+    g.gemm_testing_set_overrides()
     w = synth.BF16_WORKLOADS["qkv"]
     A, B = synth.gemm_inputs(w)
     Ad, Bd = to_dev_bf16(A), to_dev_bf16(B)

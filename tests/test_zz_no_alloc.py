@@ -5,9 +5,12 @@ framework that owns the whole device pool, a serving loop that must not call
 the CUDA allocator after warm-up, a plugin handed raw pointers but no
 allocator).  Its workspace is a fixed scratch array inside the library, so
 this test calls it straight through the C ABI, twice in a row on one stream
-with different inputs, and checks each result against the workspace-taking
-entry point, with the tolerance the other parity tests use.  It lives in a
-file of its own that pytest collects last."""
+with different inputs, and checks each result bit for bit against the
+workspace-taking entry point (same kernels, tiles and split order), which a
+partial left over from the previous call would break.  It also checks the
+size limit at its exact edge and with a split count that fits only after it
+is clamped to the K blocks.  It lives in a file of its own that pytest
+collects last."""
 from __future__ import annotations
 
 import ctypes
@@ -59,8 +62,9 @@ def test_static_scratch_splitk_twice_matches_workspace_variant(lib):
     torch.cuda.synchronize()
     assert g.gemm_get_device_status() == 0
     for C, Bh, Bd, name in ((C1, B1, B1d, "first call"), (C2, B2, B2d, "second call")):
-        ref = bits16(g.gemm_bf16_nt_splitk(Ad, Bd, splits))
-        check_close16(bits16(C), ref, K, amax(A), amax(Bh), what=f"static scratch, {name}")
+        ref = g.gemm_bf16_nt_splitk(Ad, Bd, splits)
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), f"static scratch, {name}"
+        check_close16(bits16(C), bits16(ref), K, amax(A), amax(Bh), what=f"static scratch, {name}")
     # and against the oracle, for the second call
     rows = np.arange(0, M, 37)
     check_close16(bits16(C2)[rows], oracle.gemm_bf16_nt(A, B2, rows=rows), K, amax(A), amax(B2),
@@ -71,3 +75,30 @@ def test_static_scratch_rejects_problems_over_the_limit(lib):
     # 4 splits of 4096 x 4096 FP32 partials = 256 MiB > the 32 MiB scratch
     P = 0x10000
     assert lib.gemm_bf16_nt_splitk_static(P, 2 * P, 3 * P, 4096, 4096, 4096, 4, None) == 2
+    # one 128-row tile over the limit: 2 splits x 2176 x 2048 x 4 bytes
+    assert lib.gemm_bf16_nt_splitk_static(P, 2 * P, 3 * P, 2176, 2048, 128, 2, None) == 2
+
+
+LIMIT = 32 << 20   # GEMM_SPLITK_STATIC_SCRATCH_BYTES
+
+
+@pytest.mark.parametrize("k_splits", [2, 64], ids=["exact", "clamped"])
+def test_static_scratch_at_the_limit(lib, k_splits):
+    # 2 effective splits x 2048 x 2048 x 4 bytes = exactly the 32 MiB scratch.
+    # K = 128 holds two 64-deep K blocks, so k_splits = 64 is clamped to 2:
+    # accepted only because the limit is checked on the splits actually used.
+    import nvfp4_block_scaled_tcgen05_gb300 as g
+    M, N, K = 2048, 2048, 128
+    assert g.gemm_bf16_nt_splitk_workspace_bytes(M, N, K, k_splits) == LIMIT
+    A = synth.bf16_normal((M, K), 1.0, 211)
+    B = synth.bf16_normal((N, K), 1.0, 212)
+    Ad, Bd = to_dev_bf16(A), to_dev_bf16(B)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        C.fill_(float("nan"))
+        assert lib.gemm_bf16_nt_splitk_static(Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(),
+                                              M, N, K, k_splits, stream) == 0
+        ref = g.gemm_bf16_nt_splitk(Ad, Bd, k_splits)
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    assert g.gemm_get_device_status() == 0
