@@ -95,6 +95,8 @@ def _load():
             lib.oracle_gemm_nvfp4_bs.argtypes = [u8p, u8p, u8p, u8p, u16p, L, L, L, L, lp, L, I]
             lib.oracle_gemm_w4a16.restype = I
             lib.oracle_gemm_w4a16.argtypes = [u16p, u8p, u8p, F, u16p, L, L, L, lp, L, I]
+            lib.oracle_gemm_w4a16_t.restype = I
+            lib.oracle_gemm_w4a16_t.argtypes = [u16p, u8p, u8p, F, u16p, L, L, L, L, lp, L, I]
             _lib = lib
     return _lib
 
@@ -265,3 +267,28 @@ def gemm_w4a16(A: np.ndarray, b: np.ndarray, sfb: np.ndarray, scale2: float, row
     assert rc == 0, f"oracle_gemm_w4a16 rc={rc}"
     return C
 
+
+
+def gemm_w4a16_t(A: np.ndarray, b_t: np.ndarray, sfb_t: np.ndarray, scale2: float, N: int,
+                 rows=None, threads=None) -> np.ndarray:
+    """gemm_w4a16 with the weights in the transposed layout.
+
+    b_t: uint8 [K/2, ldb], byte (j, n) = elements 2j (low nibble) and 2j+1
+    (high nibble) of weight column n; sfb_t: uint8 e4m3 [K/16, ldb], byte
+    (j, n) scaling elements 16j..16j+15 of column n; columns n >= N are
+    padding and never read.
+    """
+    A = _u16(A)
+    M, K = A.shape
+    b_t = np.ascontiguousarray(b_t, dtype=np.uint8)
+    sfb_t = np.ascontiguousarray(sfb_t, dtype=np.uint8)
+    ldb = b_t.shape[1]
+    assert b_t.shape == (K // 2, ldb) and sfb_t.shape == (K // 16, ldb) and ldb >= N
+    rp, nrows, _keep = _rows_arg(rows, M)
+    C = np.empty((nrows, N), dtype=np.uint16)
+    rc = _load().oracle_gemm_w4a16_t(_ptr(A, ctypes.c_uint16), _ptr(b_t, ctypes.c_uint8),
+                                     _ptr(sfb_t, ctypes.c_uint8), float(np.float32(scale2)),
+                                     _ptr(C, ctypes.c_uint16), M, N, K, ldb, rp, nrows,
+                                     threads or default_threads())
+    assert rc == 0, f"oracle_gemm_w4a16_t rc={rc}"
+    return C

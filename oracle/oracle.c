@@ -442,3 +442,39 @@ ORACLE_API int oracle_gemm_w4a16(const uint16_t* A, const uint8_t* b, const uint
     free(W);
     return rc;
 }
+
+/*
+ * W4A16 with the weights in the "transposed NVFP4" layout of "gemm_dense.rs"
+ * (w4a16_gemm_n128_m128_bf16 doc comment: same math as w4a16_gemm, weight
+ * layout "transposed NVFP4"; w4a16_gemm_n128_ldb doc comment: the
+ * transposed-B rows sit at r * ldb, ldb = align_up(n, 128) with the pad
+ * columns zero-filled; w4a16_gemm_n128: packed rows are exactly N apart).
+ * Reading: the byte matrix [N][K/2] of the row-oriented form, transposed:
+ *  - b_t: K/2 rows of ldb bytes; byte (j, n) holds elements k = 2j (low
+ *    nibble) and k = 2j + 1 (high nibble) of weight column n, so that a
+ *    byte stride of ldb per row makes odd N misalign 15 of every 16 rows;
+ *  - sfb_t: K/16 rows of ldb e4m3 bytes; byte (j, n) scales elements
+ *    16j .. 16j+15 of column n (the scales transposed the same way);
+ *  - bytes n >= N of a row (the padding) are never read.
+ * The arithmetic is oracle_gemm_w4a16's: w[n,k] = e2m1 * e4m3 (exact), the
+ * strict FP32 sum over k, then C = bf16(scale2 * sum).
+ * Requires K % 16 == 0 and ldb >= N.
+ */
+ORACLE_API int oracle_gemm_w4a16_t(const uint16_t* A, const uint8_t* b_t, const uint8_t* sfb_t,
+                                   float scale2, uint16_t* C, long M, long N, long K, long ldb,
+                                   const long* rows, long nrows, int threads) {
+    if (M < 0 || N < 0 || K < 0 || K % 16 || ldb < N) return -1;
+    float* W = (float*)malloc(sizeof(float) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!W) return -3;
+    for (long n = 0; n < N; ++n) {
+        for (long k = 0; k < K; ++k) {
+            uint8_t byte = b_t[(k / 2) * ldb + n];
+            unsigned code = (k % 2 == 0) ? (byte & 0x0fu) : (byte >> 4);
+            double q = oracle_e2m1_decode(code) * oracle_e4m3_decode(sfb_t[(k / 16) * ldb + n]);
+            W[n * K + k] = (float)q;        /* exact */
+        }
+    }
+    int rc = run_bf16_widened(A, W, C, M, N, K, rows, nrows, 3, scale2, threads);
+    free(W);
+    return rc;
+}

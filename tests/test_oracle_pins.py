@@ -484,3 +484,51 @@ def test_w4a16_row_selection():
     full = oracle.gemm_w4a16(A, b, sfb, scale2)
     rows = [20, 0, 7]
     assert np.array_equal(oracle.gemm_w4a16(A, b, sfb, scale2, rows=rows), full[rows])
+
+
+# --------------------------------------------------------------------------
+# W4A16 with the transposed weight layout
+# --------------------------------------------------------------------------
+
+def test_w4a16_t_layout_golden_examples():
+    with open(os.path.join(GOLDEN, "w4a16_t_layout_examples.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 5
+    for K, N, ldb, k, n, boff, nib, code, soff, sb, want in rows:
+        K, N, ldb, k, n, boff, soff = map(int, (K, N, ldb, k, n, boff, soff))
+        b_t = np.zeros((K // 2, ldb), dtype=np.uint8)
+        sfb_t = np.full((K // 16, ldb), 0x38, dtype=np.uint8)
+        c = int(code, 16)
+        b_t.reshape(-1)[boff] = c if nib == "lo" else c << 4
+        sfb_t.reshape(-1)[soff] = int(sb, 16)
+        A = np.zeros((1, K), dtype=np.uint16)
+        A[0, k] = 0x3F80
+        got = oracle.gemm_w4a16_t(A, b_t, sfb_t, 1.0, N)
+        assert int(got[0, n]) == int(want, 16), (k, n, hex(int(got[0, n])), want)
+        others = np.delete(got[0], n)
+        assert np.all((others & 0x7FFF) == 0), others   # no other column sees the weight
+
+
+@pytest.mark.parametrize("M,N,K,ldb", [(9, 32, 64, 32), (13, 37, 96, 128), (6, 129, 32, 256)])
+def test_w4a16_t_equals_row_layout_under_transpose(M, N, K, ldb):
+    # the transposed layout is the [N][K/2] byte matrix (and the [N][K/16]
+    # scale matrix) transposed, rows padded to ldb bytes with junk that must
+    # never be read
+    rng = np.random.default_rng(M + N + K)
+    w = synth.W4a16("t", M, N, K, 0.75, 95 + N)
+    A, b, sfb, scale2 = synth.w4a16_inputs(w)
+    b_t = rng.integers(0, 256, (K // 2, ldb), dtype=np.uint8)
+    sfb_t = rng.integers(0, 256, (K // 16, ldb), dtype=np.uint8)
+    b_t[:, :N] = b.T
+    sfb_t[:, :N] = sfb.T
+    want = oracle.gemm_w4a16(A, b, sfb, scale2)
+    assert np.array_equal(oracle.gemm_w4a16_t(A, b_t, sfb_t, scale2, N), want)
+    # a layout read along the wrong axis would not agree
+    if N == K // 2 and ldb == N:
+        assert not np.array_equal(oracle.gemm_w4a16_t(A, b, sfb_t, scale2, N), want)
+
+
+def test_w4a16_t_rejects_short_stride():
+    A = np.zeros((1, 32), dtype=np.uint16)
+    with pytest.raises(AssertionError):
+        oracle.gemm_w4a16_t(A, np.zeros((16, 4), np.uint8), np.zeros((2, 4), np.uint8), 1.0, 5)
