@@ -119,9 +119,10 @@ GB300GEMM_API int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_
  * A [M,K] BF16 activations; B NVFP4 packed weights: E2M1 codes, FP8 scales
  * and an FP32 per-tensor scale; C [M,N] BF16) and the doc comment of
  * w4a16_gemm_n128_m128_bf16 (FP4 dequantised to BF16, BF16 MMA, FP32
- * accumulation).  The page gives no weight layout and no place for the
- * per-tensor scale; this library reads the layout as HuggingFace-oriented
- * rows (below) and applies the scale to the FP32 sum (C is linear in it).
+ * accumulation).  This entry point takes the weights as HuggingFace-
+ * oriented rows (below); gemm_w4a16_t takes the page's transposed layout.
+ * The page gives no place for the per-tensor scale; the library applies it
+ * to the FP32 sum (C is linear in it).
  *
  *   A      bf16 [M][K], row pitch K                        (read)
  *   b      uint8 [N][K/2]: element k of row n in byte k/2, low nibble for
@@ -137,6 +138,38 @@ GB300GEMM_API int gemm_bf16_nt_scaled_acc(const void* A, const void* B, void* C_
  */
 GB300GEMM_API int gemm_w4a16(const void* A, const void* b, const void* sfb, float scale2, void* C,
                              int M, int N, int K, void* stream);
+
+/*
+ * gemm_w4a16_t - gemm_w4a16 with the weights in the transposed NVFP4 layout:
+ *     w[n,k]  = e2m1(nibble k%2 of b_t[k/2][n]) * e4m3(sfb_t[k/16][n])
+ *     C[m,n]  = bf16( scale2 * sum_k A[m,k] * w[n,k] ), FP32 accumulation
+ * Same arithmetic, same result as gemm_w4a16 on the transposed bytes.
+ *
+ * Defined by: "gemm_dense.rs", w4a16_gemm_n128_m128_bf16 doc comment (the
+ * lossless BF16 variant: same math as w4a16_gemm, weight layout "transposed
+ * NVFP4"), w4a16_gemm_n128_ldb doc comment (transposed-B rows sit r * ldb
+ * bytes apart; pass ldb = align_up(n, 128) when N is not a multiple of 16,
+ * because 16-byte copies fault on misaligned rows) and w4a16_gemm_n128
+ * (packed case: rows exactly N apart).  The library's reading: b_t is the
+ * [N][K/2] code-byte matrix of gemm_w4a16 transposed, sfb_t the [N][K/16]
+ * scale matrix transposed, both with row stride ldb.
+ *
+ *   A      bf16 [M][K], row pitch K                        (read)
+ *   b_t    uint8 [K/2][ldb]: byte (j, n) holds element 2j of weight column
+ *          n in its low nibble and element 2j+1 in its high nibble (read)
+ *   sfb_t  uint8 [K/16][ldb] e4m3: byte (j, n) scales elements 16j .. 16j+15
+ *          of column n                                     (read)
+ *   ldb    row stride of b_t and sfb_t in bytes: ldb >= N, ldb % 16 == 0;
+ *          bytes n >= N of a row are padding and never affect C
+ *   scale2 the FP32 per-tensor scale
+ *   C      bf16 [M][N], row pitch N (any N >= 1; written; must not overlap
+ *          A, b_t or sfb_t)
+ *   M, N, K >= 1; K % 128 == 0; every pointer 16-byte aligned.
+ * Errors: GEMM_ERR_NULL, _SHAPE (also ldb < N), _ALIGN (also K % 128,
+ * ldb % 16), _ALIAS, _ARCH, _LAUNCH, _NO_DEVICE.
+ */
+GB300GEMM_API int gemm_w4a16_t(const void* A, const void* b_t, const void* sfb_t, float scale2,
+                               void* C, int M, int N, int K, int ldb, void* stream);
 
 /*
  * gemm_w4a16_ws - gemm_w4a16 in two passes: the weights are first converted

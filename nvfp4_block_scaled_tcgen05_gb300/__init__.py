@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     gemm_selftest_wait_timeout,
     gemm_testing_set_overrides,
     gemm_w4a16,
+    gemm_w4a16_t,
     gemm_w4a16_ws,
     gemm_w4a16_ws_workspace_bytes,
     library_path,

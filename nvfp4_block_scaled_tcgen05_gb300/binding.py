@@ -25,7 +25,7 @@ STATUS = {
     8: "GEMM_ERR_NO_DEVICE", 9: "GEMM_ERR_CAPTURE",
 }
 EXPORTS = ("gemm_bf16_nt", "gemm_bf16_nn", "gemm_bf16_nt_scaled_acc", "gemm_bf16_nt_ordered", "gemm_nvfp4_bs",
-           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk", "gemm_w4a16", "gemm_w4a16_ws",
+           "gemm_bf16_nt_splitk", "gemm_bf16_nt_streamk", "gemm_nvfp4_bs_splitk", "gemm_w4a16", "gemm_w4a16_t", "gemm_w4a16_ws",
            "bf16_scaled_add", "gemm_get_device_status", "gemm_selftest_wait_timeout",
            "gemm_testing_set_overrides", "gemm_status_string")
 
@@ -63,6 +63,7 @@ def load() -> ctypes.CDLL:
             lib.gemm_bf16_nt_splitk_workspace_bytes.restype = ctypes.c_size_t
             lib.gemm_bf16_nt_streamk.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, vp]
             lib.gemm_w4a16.argtypes = [vp, vp, vp, f, vp, i, i, i, vp]
+            lib.gemm_w4a16_t.argtypes = [vp, vp, vp, f, vp, i, i, i, i, vp]
             lib.gemm_w4a16_ws.argtypes = [vp, vp, vp, f, vp, vp, ctypes.c_size_t, i, i, i, vp]
             lib.gemm_w4a16_ws_workspace_bytes.argtypes = [i, i]
             lib.gemm_w4a16_ws_workspace_bytes.restype = ctypes.c_size_t
@@ -242,6 +243,31 @@ def gemm_w4a16(A: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor, scale2: floa
     _mat(C, torch.bfloat16, "C")
     _check(load().gemm_w4a16(A.data_ptr(), b.data_ptr(), sfb.data_ptr(), float(scale2),
                              C.data_ptr(), M, N, K, _stream_ptr(stream)), "gemm_w4a16")
+    return C
+
+
+def gemm_w4a16_t(A: torch.Tensor, b_t: torch.Tensor, sfb_t: torch.Tensor, scale2: float, N: int,
+                 C: torch.Tensor | None = None, stream=None):
+    """gemm_w4a16 with the transposed weight layout.
+
+    A bf16 [M,K]; b_t uint8 [K/2, ldb], byte (j, n) = elements 2j (low
+    nibble) and 2j+1 (high nibble) of weight column n; sfb_t uint8 e4m3
+    [K/16, ldb]; ldb >= N (columns >= N are padding); C bf16 [M,N].
+    """
+    _mat(A, torch.bfloat16, "A")
+    _mat(b_t, torch.uint8, "b_t")
+    _mat(sfb_t, torch.uint8, "sfb_t")
+    M, K = A.shape
+    ldb = b_t.shape[1]
+    if tuple(b_t.shape) != (K // 2, ldb) or tuple(sfb_t.shape) != (K // 16, ldb):
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _mat(C, torch.bfloat16, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C must be [M, N]")
+    _check(load().gemm_w4a16_t(A.data_ptr(), b_t.data_ptr(), sfb_t.data_ptr(), float(scale2),
+                               C.data_ptr(), M, N, K, ldb, _stream_ptr(stream)), "gemm_w4a16_t")
     return C
 
 

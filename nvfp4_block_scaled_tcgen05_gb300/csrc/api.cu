@@ -279,6 +279,27 @@ int gemm_w4a16(const void* A, const void* b, const void* sfb, float scale2, void
                            scale2, C, M, N, K, dev, static_cast<cudaStream_t>(stream));
 }
 
+int gemm_w4a16_t(const void* A, const void* b_t, const void* sfb_t, float scale2, void* C, int M,
+                 int N, int K, int ldb, void* stream) {
+  if (!A || !b_t || !sfb_t || !C) return GEMM_ERR_NULL;
+  if (M <= 0 || N <= 0 || K <= 0 || ldb < N) return GEMM_ERR_SHAPE;
+  const long long tiles = (long long)((M + 255) / 256) * ((N + 255) / 256);
+  if (tiles > kMaxTiles) return GEMM_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(b_t) || !aligned16(sfb_t) || !aligned16(C))
+    return GEMM_ERR_ALIGN;
+  if (K % 128 != 0 || ldb % 16 != 0) return GEMM_ERR_ALIGN;  // whole K blocks; 16-byte rows
+  const size_t sa = size_t(M) * K * 2, sbq = size_t(K / 2) * ldb, ss = size_t(K / 16) * ldb;
+  const size_t sc = size_t(M) * N * 2;
+  if (overlaps(C, sc, A, sa) || overlaps(C, sc, b_t, sbq) || overlaps(C, sc, sfb_t, ss))
+    return GEMM_ERR_ALIAS;
+  DeviceInfo dev;
+  int rc = current_device(&dev, stream);
+  if (rc != GEMM_OK) return rc;
+  return launch_gemm_w4a16_t(A, static_cast<const uint8_t*>(b_t),
+                             static_cast<const uint8_t*>(sfb_t), scale2, C, M, N, K, ldb, dev,
+                             static_cast<cudaStream_t>(stream));
+}
+
 int gemm_w4a16_ws(const void* A, const void* b, const void* sfb, float scale2, void* C,
                   void* workspace, size_t workspace_bytes, int M, int N, int K, void* stream) {
   if (!A || !b || !sfb || !C || !workspace) return GEMM_ERR_NULL;

@@ -16,6 +16,9 @@ namespace gb300 {
 // direct-store epilogue (no output buffers): the shared memory holds the
 // code / scale ring instead
 using W4Pair = TileCfg<Operand::kW4A16, 2, 256, 3, 4, 0, true, false, 2>;
+// the transposed weight layout: the same tiles and MMA sequence with B
+// staged MN-major (as the NN GEMM stages it)
+using W4PairT = TileCfg<Operand::kW4A16, 2, 256, 3, 4, 0, true, false, 2, true>;
 
 int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2, void* C,
                       int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
@@ -53,6 +56,47 @@ int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float
   p.timeout_ns = wait_timeout_ns();
   // the A-scale map is unused; pass A's map in its place
   return launch_tcgen05<Cfg, Epilogue::kScaleBF16>(ta, tcode, tc, ta, tscale, p, dev, stream);
+}
+
+// Transposed weight layout ("gemm_dense.rs", w4a16_gemm_n128_ldb and
+// w4a16_gemm_n128_m128_bf16): codes b_t [K/2][ldb] bytes (byte (j, n) =
+// elements 2j, 2j+1 of column n), scales sfb_t [K/16][ldb]; ldb % 16 == 0,
+// K % 128 == 0, any N >= 1 (C rows are then 2N bytes apart).
+int launch_gemm_w4a16_t(const void* A, const uint8_t* b_t, const uint8_t* sfb_t, float scale2,
+                        void* C, int M, int N, int K, int ldb, const DeviceInfo& dev,
+                        cudaStream_t stream) {
+  using Cfg = W4PairT;
+  CUtensorMap ta, tcode, tscale;
+  int rc = encode_tmap_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, uint64_t(K), uint64_t(M), 1,
+                          64, Cfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // codes: K/2 rows of ldb bytes, boxes of B_ROWS columns x 64 rows (one
+  // 128-deep K block of the CTA's columns); scales: K/16 rows, 8-row boxes
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tcode, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b_t, uint64_t(ldb),
+                        uint64_t(K / 2), 1, Cfg::B_ROWS, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc == GEMM_OK)
+    rc = encode_tmap_3d(&tscale, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, sfb_t, uint64_t(ldb),
+                        uint64_t(K / 16), 1, Cfg::B_ROWS, 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != GEMM_OK) return rc;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.L = 1;
+  p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
+  p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
+  p.num_k_blocks = K / Cfg::BK;
+  p.total_tiles = p.num_m_blocks * p.num_n_blocks;
+  p.group_m = raster_group_m(p.num_m_blocks, (long long)Cfg::TILE_M * K * 2);
+  p.k_splits = 1;
+  p.kb_per_split = p.num_k_blocks;
+  p.scale = scale2;
+  p.c_ptr = C;
+  p.status = dev.status;
+  p.timeout_ns = wait_timeout_ns();
+  // the epilogue stores straight from registers: the output and A-scale
+  // maps are unused; pass A's map in their place
+  return launch_tcgen05<Cfg, Epilogue::kScaleBF16>(ta, tcode, ta, ta, tscale, p, dev, stream);
 }
 
 }  // namespace gb300

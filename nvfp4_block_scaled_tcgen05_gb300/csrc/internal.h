@@ -102,6 +102,11 @@ int launch_gemm_bf16_streamk(const void* A, const void* B, void* C, float* ws, i
 // b [N][K/2] (low nibble = even k), sfb [N][K/16]; K % 256 == 0, N % 8 == 0.
 int launch_gemm_w4a16(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2, void* C,
                       int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+// W4A16 with the transposed weight layout: b_t [K/2][ldb], sfb_t [K/16][ldb];
+// K % 128 == 0, ldb % 16 == 0, ldb >= N, any N >= 1.
+int launch_gemm_w4a16_t(const void* A, const uint8_t* b_t, const uint8_t* sfb_t, float scale2,
+                        void* C, int M, int N, int K, int ldb, const DeviceInfo& dev,
+                        cudaStream_t stream);
 // Two-pass W4A16: weights converted into ws ([N][K] BF16), then the pair GEMM
 // with the scale2 epilogue (launch_gemm_bf16_scale).
 int launch_gemm_w4a16_twopass(const void* A, const uint8_t* b, const uint8_t* sfb, float scale2,

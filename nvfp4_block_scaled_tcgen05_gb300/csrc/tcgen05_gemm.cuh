@@ -155,14 +155,24 @@ struct TileCfg {
   // B stages; DQ_WARPS warps turn each job's codes into BF16 in the B stage
   // and signal bq_full[stage] on the leader CTA (every warp of both CTAs
   // arrives).  raw_full / raw_empty pace the ring.
+  //
+  // W4A16 with B_MN (the transposed weight layout: codes stored as K/2 rows
+  // of packed bytes, byte (j, n) = elements 2j and 2j+1 of column n; scales
+  // as K/16 rows): a job's codes are one 64-row x B_ROWS-byte box, its
+  // scales one 8-row box, and the conversion warps write the weights
+  // MN-major (64-column atoms, one 128-byte row per k), the layout the NN
+  // GEMM's TMA produces.
+  static constexpr bool kW4T = kW4 && B_MN;
   static constexpr int DQ_WARPS = kW4 ? 8 : 0;
   static constexpr int DQ_ROWS = kW4 ? B_ROWS / DQ_WARPS : 0;
   static constexpr int RAW_STAGES = kW4 ? 3 : 0;
   static constexpr int RAW_CODE_BYTES = kW4 ? B_ROWS * 64 : 0;  // codes of a job
   static constexpr int RAW_BYTES = kW4 ? B_ROWS * (64 + 16) : 0;  // + the scale pairs
+  static constexpr int RAW_TX_BYTES = kW4T ? B_ROWS * (64 + 8) : RAW_BYTES;  // bytes a job loads
   static constexpr int RAW_RING_BYTES = RAW_STAGES * RAW_BYTES;
-  static_assert(!kW4 || (KSUB == 2 && !B_MN && DQ_ROWS % 8 == 0 && B_ROWS <= 256),
-                "W4A16: 128-deep stages, K-major B");
+  static_assert(!kW4 || (KSUB == 2 && DQ_ROWS % 8 == 0 && B_ROWS <= 256),
+                "W4A16: 128-deep stages");
+  static_assert(!kW4T || B_ROWS == 128, "transposed W4A16: 8 column groups of 16 per CTA");
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], epi[W][B], mma_done,
   // sf_full[S] (NVFP4) or bq_full[S], raw_full[R], raw_empty[R] (W4A16)
   static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1 +
@@ -361,6 +371,47 @@ __device__ __forceinline__ void e2m1x4_to_bf16(uint32_t g, uint32_t& w01, uint32
   hi |= (sg << 1) & 0x80808080u;  // bit 7 of a byte: bit 6 of its sg byte
   w01 = prmt(lo, hi, 0x5140u);
   w23 = prmt(lo, hi, 0x7362u);
+}
+
+// The same lookup for the transposed layout, where a byte holds two k of one
+// column: four codes (g: lo/hi nibble of column n, lo/hi nibble of column
+// n+1) -> the bf16x2 word of (k even; n, n+1) and of (k odd; n, n+1).
+__device__ __forceinline__ void e2m1x4_to_bf16_kpairs(uint32_t g, uint32_t& w_even,
+                                                      uint32_t& w_odd) {
+  constexpr uint32_t kLo0 = 0xC0800000u, kLo1 = 0xC0804000u;
+  constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;
+  const uint32_t sel = g & 0x7777u;
+  const uint32_t lo = prmt(kLo0, kLo1, sel);
+  uint32_t hi = prmt(kHi0, kHi1, sel);
+  const uint32_t sg = prmt(0u, 0x80u, (g & 0x8888u) | 0x4444u);
+  hi |= (sg << 1) & 0x80808080u;
+  w_even = prmt(lo, hi, 0x6240u);  // codes 0 and 2
+  w_odd = prmt(lo, hi, 0x7351u);   // codes 1 and 3
+}
+
+// Transposed-layout W4A16 chunk: 16 code bytes (columns n0 .. n0+15 of one
+// k pair 2j, 2j+1) and the 16 e4m3 scales of those columns -> the bf16
+// weights of row k = 2j (ev, column pairs in order) and k = 2j+1 (od).
+// Each product is exact (at most six significant bits).
+__device__ __forceinline__ void w4t_dequant_chunk(const uint4 codes, const uint4 scales,
+                                                  uint32_t (&ev)[8], uint32_t (&od)[8]) {
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+  const uint32_t sw[4] = {scales.x, scales.y, scales.z, scales.w};
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t g = (cw[p >> 1] >> (16 * (p & 1))) & 0xFFFFu;
+    const uint16_t s2 = uint16_t((sw[p >> 1] >> (16 * (p & 1))) & 0xFFFFu);
+    uint32_t s16;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(s2));
+    const __nv_bfloat162 sc =
+        __float22bfloat162_rn(__half22float2(*reinterpret_cast<const __half2*>(&s16)));
+    uint32_t we, wo;
+    e2m1x4_to_bf16_kpairs(g, we, wo);
+    const __nv_bfloat162 qe = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&we), sc);
+    const __nv_bfloat162 qo = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&wo), sc);
+    ev[p] = *reinterpret_cast<const uint32_t*>(&qe);
+    od[p] = *reinterpret_cast<const uint32_t*>(&qo);
+  }
 }
 
 __device__ __forceinline__ void w4_dequant32(const uint4 raw, uint16_t sc2, uint32_t (&out)[16]) {
@@ -595,7 +646,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
               const uint32_t da = stage_a(stage) + sub * Cfg::A_SUB_BYTES;
               const uint32_t db = stage_b(stage) + sub * Cfg::B_SUB_BYTES;
-              if constexpr (Cfg::B_MN) {
+              if constexpr (Cfg::kW4) {
+                (void)db;
+                ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
+              } else if constexpr (Cfg::B_MN) {
                 // B [K][N]: 64-column atoms of all BK rows, loaded once per stage
                 ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 if (sub == 0)
@@ -603,9 +657,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                   for (int at = 0; at < Cfg::B_ROWS / 64; ++at)
                     ptx::tma_load_3d_hint(stage_b(stage) + at * Cfg::B_ATOM_BYTES, &tmap_b, fb,
                                           b_row + 64 * at, kb * Cfg::BK, l, pol_ab);
-              } else if constexpr (Cfg::kW4) {
-                (void)db;
-                ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
               } else if constexpr (kHintLoads) {
                 ptx::tma_load_3d_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 ptx::tma_load_3d_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
@@ -639,16 +690,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
               const uint32_t da = stage_a(stage) + sub * Cfg::A_SUB_BYTES;
               const uint32_t db = stage_b(stage) + sub * Cfg::B_SUB_BYTES;
-              if constexpr (Cfg::B_MN) {
+              if constexpr (Cfg::kW4) {
+                (void)db;  // B is written by the dequantisation warps
+                ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
+              } else if constexpr (Cfg::B_MN) {
                 ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 if (sub == 0)
 #pragma unroll
                   for (int at = 0; at < Cfg::B_ROWS / 64; ++at)
                     ptx::tma_load_3d_pair_hint(stage_b(stage) + at * Cfg::B_ATOM_BYTES, &tmap_b,
                                                fb, b_row + 64 * at, kb * Cfg::BK, l, pol_ab);
-              } else if constexpr (Cfg::kW4) {
-                (void)db;  // B is written by the dequantisation warps
-                ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
               } else if constexpr (kHintLoads) {
                 ptx::tma_load_3d_pair_hint(da, &tmap_a, fb, x, a_row, l, pol_ab);
                 ptx::tma_load_3d_pair_hint(db, &tmap_b, fb, x, b_row, l, pol_ab);
@@ -717,10 +768,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             break;
           }
           const uint32_t slot = raw_base + q * Cfg::RAW_BYTES;
-          ptx::mbar_arrive_expect_tx(raw_full(q), Cfg::RAW_BYTES);
-          ptx::tma_load_3d(slot, &tmap_b, raw_full(q), kb * 64, b_row, 0);
-          ptx::tma_load_3d(slot + Cfg::RAW_CODE_BYTES, &tmap_sfb, raw_full(q), (kb & ~1) * 8,
-                           b_row, 0);
+          ptx::mbar_arrive_expect_tx(raw_full(q), Cfg::RAW_TX_BYTES);
+          if constexpr (Cfg::kW4T) {
+            // code rows kb*64 .. +63 and scale rows kb*8 .. +7, this CTA's
+            // B_ROWS columns (x in bytes = columns)
+            ptx::tma_load_3d(slot, &tmap_b, raw_full(q), b_row, kb * 64, 0);
+            ptx::tma_load_3d(slot + Cfg::RAW_CODE_BYTES, &tmap_sfb, raw_full(q), b_row, kb * 8, 0);
+          } else {
+            ptx::tma_load_3d(slot, &tmap_b, raw_full(q), kb * 64, b_row, 0);
+            ptx::tma_load_3d(slot + Cfg::RAW_CODE_BYTES, &tmap_sfb, raw_full(q), (kb & ~1) * 8,
+                             b_row, 0);
+          }
           armed |= 1u << q;
           armed_parity = (armed_parity & ~(1u << q)) | (qphase << q);
           if (++q == Cfg::RAW_STAGES) {
@@ -930,6 +988,92 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // The lanes of quarters 2 and 3 convert their two 16-element halves in
     // swapped order, which staggers the 16-byte chunks written together by
     // an 8-lane phase over all eight bank groups of a 128-byte row.
+    if constexpr (Cfg::kW4T) {
+      // Transposed weights.  A job's codes are 64 k-pair rows x 128 column
+      // bytes: 512 chunks of 16 columns, two per lane.  Lane: column group
+      // cq = lane % 8, k-pair row kk = pass * 32 + warp * 4 + lane / 8 (an
+      // 8-lane phase reads one contiguous 128-byte row).  Each chunk gives
+      // two 32-byte pieces (rows 2kk and 2kk+1) of the column group's
+      // 64-column atom; lanes of the second atom write their two 16-byte
+      // chunks in swapped order so that an 8-lane phase covers all eight
+      // bank groups.
+      constexpr int TPASSES = 64 / (Cfg::DQ_WARPS * 4);
+      const int dw = warp - (2 + Cfg::EPI_WARPS);
+      const int cq = lane & 7;
+      const int atom = cq >> 2;
+      const int c0 = (cq & 3) * 2;  // first 16-byte chunk of the group in its atom row
+      const uint32_t bq_target =
+          (CG == 2) ? ptx::mapa_shared(bq_full(0), pair_leader) : bq_full(0);
+      int stage = 0, q = 0;
+      uint32_t phase = 0, qphase = 0;
+      bool ok = true;
+      Seg sg;
+      for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          if (!__all_sync(0xffffffffu, wait_bar(raw_full(q), qphase, w, 8))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* slot = smem + (raw_base - sbase) + q * Cfg::RAW_BYTES;
+          uint4 codes[TPASSES], scl[TPASSES];
+#pragma unroll
+          for (int ps = 0; ps < TPASSES; ++ps) {
+            const int kk = ps * (Cfg::DQ_WARPS * 4) + dw * 4 + (lane >> 3);
+            codes[ps] = *reinterpret_cast<const uint4*>(slot + kk * Cfg::B_ROWS + cq * 16);
+            scl[ps] = *reinterpret_cast<const uint4*>(slot + Cfg::RAW_CODE_BYTES +
+                                                      (kk >> 3) * Cfg::B_ROWS + cq * 16);
+          }
+          // The slot is refilled by TMA (the async proxy): order these
+          // generic reads before that write.  Without the fence a load still
+          // in flight at the release can return the next job's bytes.
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(raw_empty(q));
+          if (++q == Cfg::RAW_STAGES) {
+            q = 0;
+            qphase ^= 1u;
+          }
+          if (!__all_sync(0xffffffffu, wait_bar(empty_bar(stage), phase ^ 1u, w, 11))) {
+            ok = false;
+            break;
+          }
+          uint8_t* atom_base = smem + (stage_b(stage) - sbase) + atom * Cfg::B_ATOM_BYTES;
+#pragma unroll
+          for (int ps = 0; ps < TPASSES; ++ps) {
+            uint32_t ev[8], od[8];
+            w4t_dequant_chunk(codes[ps], scl[ps], ev, od);
+            const int kk = ps * (Cfg::DQ_WARPS * 4) + dw * 4 + (lane >> 3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // rows 2kk (even) and 2kk+1 (odd)
+              const int k = 2 * kk + h;
+              const uint32_t* v = h ? od : ev;  // h is a compile-time index
+              uint8_t* rowp = atom_base + k * 128;
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                // half `part` of the group (columns 0-7 / 8-15); selects keep
+                // the register indices static
+                const int part = i ^ atom;
+                const uint4 val = atom ? make_uint4(v[4 * (1 - i)], v[4 * (1 - i) + 1],
+                                                    v[4 * (1 - i) + 2], v[4 * (1 - i) + 3])
+                                       : make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                                                    v[4 * i + 3]);
+                *reinterpret_cast<uint4*>(rowp + (((c0 + part) ^ (k & 7)) << 4)) = val;
+              }
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 2) ptx::mbar_arrive_remote(bq_target + 8 * stage);
+            else ptx::mbar_arrive(bq_full(stage));
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    } else {
     constexpr int PASSES = Cfg::kW4 ? Cfg::DQ_ROWS / 8 : 1;
     const int dw = warp - (2 + Cfg::EPI_WARPS);
     const int prow = lane >> 2;
@@ -962,6 +1106,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           codes[ps] = c;
           scl[ps] = sv;
         }
+        // generic reads of a slot that TMA refills: fence before the release
+        ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(raw_empty(q));
         if (++q == Cfg::RAW_STAGES) {
@@ -997,6 +1143,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           phase ^= 1u;
         }
       }
+    }
     }
   } else if (warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
@@ -1210,12 +1357,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (grow >= p.M || col0 >= p.N) continue;
           uint16_t* dst = static_cast<uint16_t*>(p.c_ptr) +
                           (size_t(l) * p.M + size_t(grow)) * size_t(p.N) + col0;
+          if ((p.N & 7) == 0) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (col0 + 8 * j >= p.N) break;
-            const uint32_t* v = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
-            const uint4 o = epi_chunk<EPI>(v, make_uint4(0, 0, 0, 0), p.scale);
-            *reinterpret_cast<uint4*>(dst + 8 * j) = o;
+            for (int j = 0; j < 8; ++j) {
+              if (col0 + 8 * j >= p.N) break;
+              const uint32_t* v = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
+              const uint4 o = epi_chunk<EPI>(v, make_uint4(0, 0, 0, 0), p.scale);
+              *reinterpret_cast<uint4*>(dst + 8 * j) = o;
+            }
+          } else {
+            // N not a multiple of 8 (rows are not 16-byte aligned): 2-byte
+            // stores, none past column N-1
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t* v = (j < 4) ? &r0[8 * j] : &r1[8 * (j - 4)];
+              const uint4 o = epi_chunk<EPI>(v, make_uint4(0, 0, 0, 0), p.scale);
+              const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col0 + 8 * j + e < p.N)
+                  dst[8 * j + e] = uint16_t(ow[e >> 1] >> (16 * (e & 1)));
+            }
           }
         }
       } else {

@@ -229,3 +229,26 @@ def test_w4a16_ws_workspace_and_arguments(lib):
     assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 5 * P + 8, big, 8, 8, 256, None) == 3   # misaligned
     assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 5 * P, 16, 8, 8, 256, None) == 2        # too small
     assert f(P, 2 * P, 3 * P, 1.0, 4 * P, 4 * P + 16, big, 8, 8, 256, None) == 4  # on C
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, 2 * P, 3 * P, 1.0, 4 * P, 8, 8, 128, 16), 1),         # NULL A
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 8, 8, 128, 0), 2),          # ldb < N
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 8, 0, 128, 16), 2),         # N = 0
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 8, 9, 128, 24), 3),         # ldb % 16 != 0
+    ((P, 2 * P, 3 * P, 1.0, 4 * P, 8, 9, 192, 16), 3),         # K % 128 != 0
+    ((P, 2 * P + 8, 3 * P, 1.0, 4 * P, 8, 9, 128, 16), 3),     # misaligned b_t
+    ((P, 2 * P, 3 * P, 1.0, 2 * P + 64, 8, 9, 128, 16), 4),    # C overlaps b_t
+])
+def test_w4a16_t_rejects_bad_arguments(lib, args, expect):
+    f = lib.gemm_w4a16_t
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.c_void_p] + [ctypes.c_int] * 4 + \
+        [ctypes.c_void_p]
+    assert f(*args, None) == expect
+
+
+def test_testing_overrides_reject_bad_values(lib):
+    f = lib.gemm_testing_set_overrides
+    f.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert f(3, 0) == 2 and f(0, -1) == 2
+    assert f(0, 0) == 0
