@@ -55,6 +55,9 @@ def parse():
                     help="comma list of the extra shapes to measure")
     ap.add_argument("--no-headline", action="store_true",
                     help="profiling aid: measure only --shapes and print them")
+    ap.add_argument("--tensor-rate", action="store_true",
+                    help="measure the tcgen05 MMA issue rate (BF16 and block-scaled FP4) with "
+                         "the probe library and print it, instead of the GEMM benchmark")
     return ap.parse_args()
 
 
@@ -254,11 +257,73 @@ def run_reference(args):
     }))
 
 
+# ----------------------------------------------------------------- tensor rate
+def tensor_rate(torch, dev, local, n_mma=8192):
+    """SM cycles per CTA-pair MMA issued back to back by one thread (zero
+    operands in shared memory), for kind::f16 256x256x16 and
+    kind::mxf4nvf4 256x256x64, alone on one CTA pair and on every SM pair,
+    and with tcgen05.cp scale copies issued by two other warps at the same
+    time (copies per 4 MMAs).  Whole-GPU rates use CUDA events around the
+    launch and the SM clock sampled meanwhile."""
+    import ctypes
+    from nvfp4_block_scaled_tcgen05_gb300 import build as _b
+    lib = ctypes.CDLL(_b.PROBE_LIB)
+    f = lib.probe_tensor_rate
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    props = torch.cuda.get_device_properties(dev)
+    pairs = props.multi_processor_count // 2
+    out = torch.zeros(2 * pairs, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    rows = []
+    flops = {0: 2.0 * 256 * 256 * 16, 1: 2.0 * 256 * 256 * 64}
+    for kind, copies in ((0, 0), (1, 0), (1, 2), (1, 8), (1, 10), (1, 12)):
+        for clusters in (1, pairs):
+            for _ in range(2):  # warm-up launch, then the measured one
+                rc = f(kind, clusters, n_mma, copies, out.data_ptr(), stream)
+                if rc:
+                    raise RuntimeError(f"probe_tensor_rate rc={rc}")
+            clocks = ClockSampler(local)
+            clocks.start()
+            time.sleep(0.15)
+            t0 = time.time()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 20 if clusters > 1 else 3
+            e0.record()
+            for _ in range(reps):
+                f(kind, clusters, n_mma, copies, out.data_ptr(), stream)
+            e1.record()
+            e1.synchronize()
+            t1 = time.time()
+            clocks.stop()
+            clk = clocks.summary(t0, t1)
+            v = out.view(pairs, 2)[:clusters].cpu().numpy()
+            cyc = v[:, 0].astype(np.float64) / n_mma
+            sec = e0.elapsed_time(e1) / 1e3 / reps
+            rows.append({"kind": "bf16 kind::f16 256x256x16" if kind == 0
+                         else "nvfp4 kind::mxf4nvf4 4X 256x256x64",
+                         "copies_per_4_mma": copies, "cta_pairs": clusters,
+                         "cycles_per_mma_median": float(np.median(cyc)),
+                         "cycles_per_mma_max": float(cyc.max()),
+                         "flop_per_sm_per_cycle": flops[kind] / 2 / float(np.median(cyc)),
+                         "tflops_whole_launch": clusters * n_mma * flops[kind] / sec / 1e12,
+                         "sm_mhz_median": clk.get("sm_mhz")})
+    return rows
+
+
 # ----------------------------------------------------------------- our arm
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.tensor_rate:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        print(json.dumps({"tensor_rate": tensor_rate(torch, torch.device("cuda", local), local)}))
         return
     import torch
     import torch.distributed as dist

@@ -1,7 +1,9 @@
 """Builds libgb300gemm.so in-tree with nvcc for sm_103a (one -gencode).
 
 Each .cu in csrc/ is compiled to an object in parallel, then the objects are
-linked into a shared library next to this file.  The build is skipped when
+linked into a shared library next to this file.  The measurement tool in
+probe/ (tensor-pipe issue rate, used by bench.py --tensor-rate) is linked
+into libgb300probe.so beside it.  The build is skipped when
 the library is newer than every source and header.
 """
 from __future__ import annotations
@@ -15,9 +17,12 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
+PROBE = os.path.join(PKG, "probe")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build", "gb300gemm")
 LIB = os.path.join(PKG, "libgb300gemm.so")
+# measurement tool (tensor-pipe issue rate), kept out of the GEMM library
+PROBE_LIB = os.path.join(PKG, "libgb300probe.so")
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
@@ -43,24 +48,27 @@ def sources():
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files += [os.path.join(PROBE, f) for f in os.listdir(PROBE)]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(PROBE_LIB)):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(PROBE_LIB))
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
 def _compile(nvcc: str, src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(OBJDIR, src[:-3] + ".o")
+    """src: a file name in csrc/, or 'probe/<name>' for the measurement tool."""
+    path = os.path.join(PKG, src) if src.startswith("probe/") else os.path.join(CSRC, src)
+    obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc, *GENCODE, *NVCC_FLAGS, *EXTRA.get(src, [])]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
-    cmd += ["-c", os.path.join(CSRC, src), "-o", obj]
+    cmd += ["-c", path, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -76,14 +84,17 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     nvcc = nvcc_path()
     os.makedirs(OBJDIR, exist_ok=True)
     srcs = sources()
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(nvcc, s, verbose_ptxas), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *GENCODE, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    probes = ["probe/" + f for f in sorted(os.listdir(PROBE)) if f.endswith(".cu")]
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs) + len(probes),
+                                                      os.cpu_count() or 1))) as ex:
+        objs = list(ex.map(lambda s: _compile(nvcc, s, verbose_ptxas), srcs + probes))
+    for lib, parts in ((LIB, objs[:len(srcs)]), (PROBE_LIB, objs[len(srcs):])):
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc, *GENCODE, "-shared", "-cudart", "static", "-o", tmp, *parts]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 
