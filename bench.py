@@ -260,27 +260,45 @@ def run_reference(args):
 # ----------------------------------------------------------------- tensor rate
 def tensor_rate(torch, dev, local, n_mma=8192):
     """SM cycles per CTA-pair MMA issued back to back by one thread (zero
-    operands in shared memory), for kind::f16 256x256x16 and
-    kind::mxf4nvf4 256x256x64, alone on one CTA pair and on every SM pair,
-    and with tcgen05.cp scale copies issued by two other warps at the same
-    time (copies per 4 MMAs).  Whole-GPU rates use CUDA events around the
-    launch and the SM clock sampled meanwhile."""
+    operands in shared memory), for kind::f16 256xNx16 and kind::mxf4nvf4
+    256xNx64 (N = 256: the square tiles; N = 128: the decode tiles), alone on
+    one CTA pair and on every SM pair, and with tcgen05.cp scale copies
+    issued by two other warps at the same time (per 4 MMAs: `copies`
+    32x128b.warpx4 and `wide` 128x256b; the decode kernel's mix is 4 + 2).
+    With `commit_every` the issuers also commit per stage as the GEMM
+    kernel does (the MMA thread every 4 MMAs; the copy warps after each
+    group); `flags` place waiting threads beside the MMAs (bit meanings in
+    probe/tensor_rate.cu: 1 multicast commits, 2 a polling thread on the
+    peer CTA, 4 that poll sleeps, 8/16 one lane / a whole warp of the MMA
+    CTA polling, 32 that poll sleeps, 64 / 128 commits in a fixed pattern
+    after each group of 4 MMAs / after the next group's first MMA).
+    Whole-GPU rates use CUDA events around
+    the launch and the SM clock sampled meanwhile."""
     import ctypes
     from nvfp4_block_scaled_tcgen05_gb300 import build as _b
     lib = ctypes.CDLL(_b.PROBE_LIB)
     f = lib.probe_tensor_rate
-    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    f.argtypes = [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_void_p]
     f.restype = ctypes.c_int
     props = torch.cuda.get_device_properties(dev)
     pairs = props.multi_processor_count // 2
     out = torch.zeros(2 * pairs, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     rows = []
-    flops = {0: 2.0 * 256 * 256 * 16, 1: 2.0 * 256 * 256 * 64}
-    for kind, copies in ((0, 0), (1, 0), (1, 2), (1, 8), (1, 10), (1, 12)):
+    kdepth = {0: 16, 1: 64}
+    cases = ((0, 256, 0, 0, 0, 0), (1, 256, 0, 0, 0, 0), (1, 256, 8, 0, 0, 0),
+             (1, 256, 12, 0, 0, 0), (1, 256, 0, 0, 0, 2), (1, 256, 0, 0, 0, 24),
+             (1, 256, 0, 0, 4, 0), (1, 256, 0, 0, 64, 0), (1, 256, 0, 0, 4096, 0),
+             (1, 256, 0, 0, 4, 64), (1, 256, 0, 0, 4, 128), (1, 256, 0, 0, 4, 65),
+             (1, 256, 0, 0, 4, 129), (1, 256, 8, 0, 4, 129), (0, 256, 0, 0, 4, 64),
+             (0, 128, 0, 0, 0, 0), (1, 128, 0, 0, 0, 0), (1, 128, 4, 2, 0, 0),
+             (1, 128, 4, 2, 4, 64), (1, 128, 4, 2, 4, 129))
+    for kind, mma_n, copies, wide, commit_every, flags in cases:
+        flops = 2.0 * 256 * mma_n * kdepth[kind]
         for clusters in (1, pairs):
             for _ in range(2):  # warm-up launch, then the measured one
-                rc = f(kind, clusters, n_mma, copies, out.data_ptr(), stream)
+                rc = f(kind, mma_n, clusters, n_mma, copies, wide, commit_every, flags,
+                       out.data_ptr(), stream)
                 if rc:
                     raise RuntimeError(f"probe_tensor_rate rc={rc}")
             clocks = ClockSampler(local)
@@ -291,7 +309,8 @@ def tensor_rate(torch, dev, local, n_mma=8192):
             reps = 20 if clusters > 1 else 3
             e0.record()
             for _ in range(reps):
-                f(kind, clusters, n_mma, copies, out.data_ptr(), stream)
+                f(kind, mma_n, clusters, n_mma, copies, wide, commit_every, flags, out.data_ptr(),
+                  stream)
             e1.record()
             e1.synchronize()
             t1 = time.time()
@@ -300,13 +319,15 @@ def tensor_rate(torch, dev, local, n_mma=8192):
             v = out.view(pairs, 2)[:clusters].cpu().numpy()
             cyc = v[:, 0].astype(np.float64) / n_mma
             sec = e0.elapsed_time(e1) / 1e3 / reps
-            rows.append({"kind": "bf16 kind::f16 256x256x16" if kind == 0
-                         else "nvfp4 kind::mxf4nvf4 4X 256x256x64",
-                         "copies_per_4_mma": copies, "cta_pairs": clusters,
+            rows.append({"kind": (f"bf16 kind::f16 256x{mma_n}x16" if kind == 0
+                                  else f"nvfp4 kind::mxf4nvf4 4X 256x{mma_n}x64"),
+                         "copies_per_4_mma": copies, "wide_copies_per_4_mma": wide,
+                         "commit_every": commit_every, "flags": flags,
+                         "cta_pairs": clusters,
                          "cycles_per_mma_median": float(np.median(cyc)),
                          "cycles_per_mma_max": float(cyc.max()),
-                         "flop_per_sm_per_cycle": flops[kind] / 2 / float(np.median(cyc)),
-                         "tflops_whole_launch": clusters * n_mma * flops[kind] / sec / 1e12,
+                         "flop_per_sm_per_cycle": flops / 2 / float(np.median(cyc)),
+                         "tflops_whole_launch": clusters * n_mma * flops / sec / 1e12,
                          "sm_mhz_median": clk.get("sm_mhz")})
     return rows
 

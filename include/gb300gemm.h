@@ -340,11 +340,14 @@ GB300GEMM_API int gemm_nvfp4_bs(const void* a, const void* b, const void* sfa, c
                   int L, int M, int N, int K, void* stream);
 
 /*
- * gemm_nvfp4_bs_splitk - gemm_nvfp4_bs for L == 1 with K split into
- * `k_splits` chunks, for problems with too few output tiles to fill the GPU
+ * gemm_nvfp4_bs_splitk - gemm_nvfp4_bs with K split into `k_splits`
+ * chunks, for problems with too few output tiles to fill the GPU
  * (decode-like M = 128): each chunk's FP32 partial product goes into
- * workspace[s][M][N], then the chunks are summed in split order in FP32
- * (deterministic) and rounded once to FP16.
+ * workspace[s][l][M][N], then the chunks are summed in split order in FP32
+ * (deterministic) and rounded once to FP16.  With M <= 256 the kernel swaps
+ * the operand roles (the weight rows b take the MMA's 256-row side of a CTA
+ * pair, the activation rows the MMA N) and stores the partials transposed;
+ * the result is the same product.
  *
  * Defined by: the operation is gemm_nvfp4_bs's ("kernelbot nvfp4 gemm
  * submission 123329", custom_kernel and the docstring's layout sections;
@@ -352,25 +355,26 @@ GB300GEMM_API int gemm_nvfp4_bs(const void* a, const void* b, const void* sfa, c
  * split-K scheme is "gemm_dense.rs", dense_gemm_splitk (FP32 partials over
  * K chunks, then a reduce).
  *
- *   a, b, sfa, sfb, c: as gemm_nvfp4_bs with L = 1.
+ *   a, b, sfa, sfb, c, L, M, N, K: as gemm_nvfp4_bs (L >= 1).
  *   K is split in 256-element blocks: S = min(k_splits, K/256), reduced so
  *   that every chunk is non-empty (gemm_nvfp4_bs_splitk_workspace_bytes
- *   gives S*M*N*4 for the S used).
+ *   gives S*M*N*4 for the S used, per batch).
  *   workspace: caller-owned device memory of at least
- *   gemm_nvfp4_bs_splitk_workspace_bytes(M,N,K,k_splits) bytes, 16-byte
+ *   L * gemm_nvfp4_bs_splitk_workspace_bytes(M,N,K,k_splits) bytes, 16-byte
  *   aligned, overlapping no operand; contents on entry are ignored, on
  *   return unspecified.  1 <= k_splits <= 64.
  * The FP32 sum order differs from gemm_nvfp4_bs (per chunk, then across
  * chunks), so results may differ from it in the last FP16 bit.
- * Errors: as gemm_nvfp4_bs; GEMM_ERR_SHAPE also for L != 1, a bad k_splits
- * or a workspace that is too small; GEMM_ERR_NULL for a NULL workspace.
+ * Errors: as gemm_nvfp4_bs; GEMM_ERR_SHAPE also for a bad k_splits or a
+ * workspace that is too small; GEMM_ERR_NULL for a NULL workspace.
  */
 GB300GEMM_API int gemm_nvfp4_bs_splitk(const void* a, const void* b, const void* sfa,
                                        const void* sfb, void* c, void* workspace,
                                        size_t workspace_bytes, int L, int M, int N, int K,
                                        int k_splits, void* stream);
 
-/* Workspace bytes gemm_nvfp4_bs_splitk needs (0 for invalid arguments). */
+/* Workspace bytes gemm_nvfp4_bs_splitk needs per batch (0 for invalid
+ * arguments); an L-batch call needs L times this. */
 GB300GEMM_API size_t gemm_nvfp4_bs_splitk_workspace_bytes(int M, int N, int K, int k_splits);
 
 /*

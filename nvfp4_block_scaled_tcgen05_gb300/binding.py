@@ -345,27 +345,27 @@ def gemm_nvfp4_bs_splitk_workspace_bytes(M: int, N: int, K: int, k_splits: int) 
 def gemm_nvfp4_bs_splitk(a: torch.Tensor, b: torch.Tensor, sfa: torch.Tensor, sfb: torch.Tensor,
                          M: int, N: int, K: int, k_splits: int,
                          workspace: torch.Tensor | None = None, c: torch.Tensor | None = None,
-                         stream=None):
-    """fp16 c[1,M,N] = gemm_nvfp4_bs with K split into k_splits chunks (L = 1)."""
+                         stream=None, L: int = 1):
+    """fp16 c[L,M,N] = gemm_nvfp4_bs with K split into k_splits chunks."""
     for t, n in ((a, "a"), (b, "b"), (sfa, "sfa"), (sfb, "sfb")):
         if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_cuda or not t.is_contiguous():
             raise TypeError(f"{n} must be a contiguous CUDA uint8 tensor")
-    if a.numel() != M * K // 2 or b.numel() != N * K // 2:
+    if a.numel() != L * M * K // 2 or b.numel() != L * N * K // 2:
         raise ValueError("a/b size mismatch")
-    if sfa.numel() != M * K // 16 or sfb.numel() != N * K // 16:
+    if sfa.numel() != L * M * K // 16 or sfb.numel() != L * N * K // 16:
         raise ValueError("scale buffer size mismatch")
-    need = gemm_nvfp4_bs_splitk_workspace_bytes(M, N, K, k_splits)
+    need = L * gemm_nvfp4_bs_splitk_workspace_bytes(M, N, K, k_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=a.device)
     if not (workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
     if c is None:
-        c = torch.empty((1, M, N), dtype=torch.float16, device=a.device)
-    if c.dtype != torch.float16 or not c.is_contiguous() or c.numel() != M * N:
-        raise ValueError("c must be a contiguous fp16 [1, M, N] tensor")
+        c = torch.empty((L, M, N), dtype=torch.float16, device=a.device)
+    if c.dtype != torch.float16 or not c.is_contiguous() or c.numel() != L * M * N:
+        raise ValueError("c must be a contiguous fp16 [L, M, N] tensor")
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().gemm_nvfp4_bs_splitk(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
-                                       c.data_ptr(), workspace.data_ptr(), nbytes, 1, M, N, K,
+                                       c.data_ptr(), workspace.data_ptr(), nbytes, L, M, N, K,
                                        int(k_splits), _stream_ptr(stream)), "gemm_nvfp4_bs_splitk")
     return c
 

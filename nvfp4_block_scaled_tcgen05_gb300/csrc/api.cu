@@ -372,21 +372,21 @@ int gemm_nvfp4_bs_splitk(const void* a, const void* b, const void* sfa, const vo
                          void* workspace, size_t workspace_bytes, int L, int M, int N, int K,
                          int k_splits, void* stream) {
   if (!a || !b || !sfa || !sfb || !c || !workspace) return GEMM_ERR_NULL;
-  if (L != 1 || M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_SHAPE;
+  if (L <= 0 || M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_SHAPE;
   if (M % 128 != 0 || N % 128 != 0 || K % 256 != 0) return GEMM_ERR_SHAPE;
   if (k_splits < 1 || k_splits > 64) return GEMM_ERR_SHAPE;
   int kbps = 0;
   const int s_eff = nvfp4_splitk_effective_splits(K, k_splits, &kbps);
-  const long long units = (long long)s_eff * (M / 128) * ((N + 255) / 256);
+  const long long units = (long long)s_eff * L * ((M + 255) / 256) * ((N + 255) / 256);
   if (units > kMaxTiles) return GEMM_ERR_SHAPE;
-  const size_t need = size_t(s_eff) * size_t(M) * size_t(N) * 4;
+  const size_t need = size_t(s_eff) * size_t(L) * size_t(M) * size_t(N) * 4;
   if (workspace_bytes < need) return GEMM_ERR_SHAPE;
   if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(c) ||
       !aligned16(workspace))
     return GEMM_ERR_ALIGN;
-  const size_t sa = size_t(M) * (K / 2), sb = size_t(N) * (K / 2);
-  const size_t ssa = size_t(M) * (K / 16), ssb = size_t(N) * (K / 16);
-  const size_t sc = size_t(M) * N * 2;
+  const size_t sa = size_t(L) * M * (K / 2), sb = size_t(L) * N * (K / 2);
+  const size_t ssa = size_t(L) * M * (K / 16), ssb = size_t(L) * N * (K / 16);
+  const size_t sc = size_t(L) * M * N * 2;
   if (overlaps(c, sc, a, sa) || overlaps(c, sc, b, sb) || overlaps(c, sc, sfa, ssa) ||
       overlaps(c, sc, sfb, ssb))
     return GEMM_ERR_ALIAS;
@@ -397,7 +397,7 @@ int gemm_nvfp4_bs_splitk(const void* a, const void* b, const void* sfa, const vo
   DeviceInfo dev;
   int rc = current_device(&dev, stream);
   if (rc != GEMM_OK) return rc;
-  return launch_gemm_nvfp4_splitk(a, b, sfa, sfb, c, static_cast<float*>(workspace), M, N, K,
+  return launch_gemm_nvfp4_splitk(a, b, sfa, sfb, c, static_cast<float*>(workspace), L, M, N, K,
                                   k_splits, dev, static_cast<cudaStream_t>(stream));
 }
 

@@ -30,15 +30,23 @@
 // (cta_group::1, 128 x 256 tiles, 3 stages, scale-copy warps) faulted the
 // GPU twice when launched back to back; the cause was not found, so it is
 // not used.
-// Split-K (decode-like M = 128 with few output tiles): the pair
-// configuration writes FP32 partials of K-block chunks straight from
-// registers into a caller workspace, then an ordered reduce rounds once to
-// FP16 ("gemm_dense.rs", dense_gemm_splitk, applied to the block-scaled GEMM).
+// Split-K (decode-like M = 128 with few output tiles): FP32 partials of
+// K-block chunks go straight from registers into a caller workspace, then an
+// ordered reduce rounds once to FP16 ("gemm_dense.rs", dense_gemm_splitk,
+// applied to the block-scaled GEMM).  With M <= 256 the operands swap roles
+// (D = B . A^T, the weights on the 256-row MMA side of the CTA pair, the
+// activation rows as MMA N = 128) and the epilogue stores D transposed: no
+// MMA rows are spent on zero fill, and the 256-row weight tiles times the
+// splits give enough work units for every CTA pair.
 #include "launch.cuh"
 
 namespace gb300 {
 
 using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 0, true, false>;
+// Decode-like problems (M <= 256 activation rows): the operands swap roles,
+// so the weights fill the 256-row MMA M side of a CTA pair and the
+// activation rows are the MMA N = 128; the output is stored transposed.
+using Nvfp4PairT = TileCfg<Operand::kNVFP4, 2, 128, 6, 4, 0, true, false, 1, false, true>;
 
 // `out` is the FP16 output (EPI = kStoreFP16) or, with splits > 1 (L = 1),
 // the FP32 workspace [splits][M][N] (EPI = kStoreF32).
@@ -83,7 +91,7 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
   p.M = M;
   p.N = N;
   p.K = K;
-  p.L = splits > 1 ? splits : L;  // with split-K the batch slot indexes the split
+  p.L = splits > 1 ? splits * L : L;  // split-K: batch slot = batch * splits + split
   p.num_m_blocks = (M + Cfg::TILE_M - 1) / Cfg::TILE_M;
   p.num_n_blocks = (N + Cfg::BN - 1) / Cfg::BN;
   p.num_k_blocks = K / Cfg::BK;
@@ -100,6 +108,8 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
   return launch_tcgen05<Cfg, EPI>(ta, tb, tc, tsa, tsb, p, dev, stream);
 }
 
+constexpr int kNvfp4SwapMaxM = 256;  // activation rows up to this use the swapped kernel
+
 int launch_gemm_nvfp4(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
                       int L, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   return run_nvfp4<Nvfp4Pair>(a, b, sfa, sfb, c, L, M, N, K, 1, 0, dev, stream);
@@ -114,14 +124,19 @@ int nvfp4_splitk_effective_splits(int K, int splits, int* kb_per_split) {
 }
 
 int launch_gemm_nvfp4_splitk(const void* a, const void* b, const void* sfa, const void* sfb,
-                             void* c, float* ws, int M, int N, int K, int splits,
+                             void* c, float* ws, int L, int M, int N, int K, int splits,
                              const DeviceInfo& dev, cudaStream_t stream) {
   int kbps = 0;
   const int s_eff = nvfp4_splitk_effective_splits(K, splits, &kbps);
-  const int rc = run_nvfp4<Nvfp4Pair, Epilogue::kStoreF32>(a, b, sfa, sfb, ws, 1, M, N, K, s_eff,
-                                                            kbps, dev, stream);
+  // partials ws[split][batch][M][N] in FP32, either orientation
+  const int rc =
+      (M <= kNvfp4SwapMaxM)
+          ? run_nvfp4<Nvfp4PairT, Epilogue::kStoreF32>(b, a, sfb, sfa, ws, L, N, M, K, s_eff, kbps,
+                                                        dev, stream)
+          : run_nvfp4<Nvfp4Pair, Epilogue::kStoreF32>(a, b, sfa, sfb, ws, L, M, N, K, s_eff, kbps,
+                                                       dev, stream);
   if (rc != GEMM_OK) return rc;
-  return launch_splitk_reduce_f16(ws, c, size_t(M) * N, s_eff, dev, stream);
+  return launch_splitk_reduce_f16(ws, c, size_t(L) * M * N, s_eff, dev, stream);
 }
 
 }  // namespace gb300

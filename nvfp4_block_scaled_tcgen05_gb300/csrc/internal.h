@@ -85,12 +85,12 @@ int launch_selftest_timeout(int timeout_ms, const DeviceInfo& dev, cudaStream_t 
 int splitk_effective_splits(int K, int splits, int* kb_per_split);
 int launch_gemm_bf16_splitk(const void* A, const void* B, void* C, float* ws, int M, int N, int K,
                             int splits, const DeviceInfo& dev, cudaStream_t stream);
-// NVFP4 split-K (L == 1): S = min(k_splits, K/256) chunks of whole 256-deep
-// K blocks, reduced so every chunk is non-empty; FP32 partials in
-// ws[S][M][N], then an ordered reduce to FP16.
+// NVFP4 split-K: S = min(k_splits, K/256) chunks of whole 256-deep K
+// blocks, reduced so every chunk is non-empty; FP32 partials in
+// ws[S][L][M][N], then an ordered reduce to FP16.
 int nvfp4_splitk_effective_splits(int K, int splits, int* kb_per_split);
 int launch_gemm_nvfp4_splitk(const void* a, const void* b, const void* sfa, const void* sfb,
-                             void* c, float* ws, int M, int N, int K, int splits,
+                             void* c, float* ws, int L, int M, int N, int K, int splits,
                              const DeviceInfo& dev, cudaStream_t stream);
 // Stream-K (CTA pairs, 256 x 256 tiles): at most streamk_max_clusters(dev)
 // clusters, each with two FP32 partial tiles of workspace.

@@ -55,8 +55,9 @@ struct GemmParams {
   int M, N, K, L;                 // K in elements
   int num_m_blocks, num_n_blocks, num_k_blocks, total_tiles;
   int rest_m, rest_n, rest_k;     // NVFP4 scale layout extents: M/128, N/128, K/64
-  int k_splits, kb_per_split;     // split-K: the batch index l selects K blocks
-                                  // [l*kb_per_split, (l+1)*kb_per_split); 1 / num_k_blocks otherwise
+  int k_splits, kb_per_split;     // split-K: batch slot l = batch * k_splits + split; the
+                                  // split selects K blocks [split*kb_per_split, +kb_per_split);
+                                  // 1 / num_k_blocks otherwise
   float scale;                    // scaled-acc factor
   void* c_ptr;                    // output base (direct-store epilogue only)
   unsigned int* status;           // device status word
@@ -66,7 +67,8 @@ struct GemmParams {
 };
 
 template <Operand OP, int CG_, int BN_, int STAGES_, int EPI_WARPS_ = 4, int EPI_BUFS_ = 2,
-          bool SFA_REP_ = true, bool SFB_REP_ = false, int KSUB_ = 1, bool B_MN_ = false>
+          bool SFA_REP_ = true, bool SFB_REP_ = false, int KSUB_ = 1, bool B_MN_ = false,
+          bool C_T_ = false>
 struct TileCfg {
   static constexpr Operand kOp = OP;
   static constexpr bool kFP4 = (OP == Operand::kNVFP4);
@@ -92,6 +94,9 @@ struct TileCfg {
   // the CTA's B columns as 64-column atoms (BK rows of 128 bytes each, the
   // TMA's 128-byte swizzle), and the MMA reads B MN-major.
   static constexpr bool B_MN = B_MN_;
+  // C_T: the output is D transposed (the swapped-operand decode GEMM, whose
+  // M role holds the weights and N role the few activation rows)
+  static constexpr bool C_T = C_T_;
   static constexpr int BK = kFP4 ? 256 : 64 * KSUB;  // K elements per stage
   static constexpr int KX = kFP4 ? 128 : 64;      // TMA x-extent per sub-tile (bytes or elements)
   static constexpr int MMA_K = kFP4 ? 64 : 16;    // K per MMA = 32 bytes per row
@@ -244,7 +249,7 @@ __device__ __forceinline__ bool seg_at(const GemmParams& p, int c, int C, int id
     if (p.k_splits > 1) {
       int l, mb, nb;
       decode_tile<Cfg>(s.tile, p, l, mb, nb);
-      s.kb0 = l * p.kb_per_split;
+      s.kb0 = (l % p.k_splits) * p.kb_per_split;
       s.kb1 = min(p.num_k_blocks, s.kb0 + p.kb_per_split);
     }
     return true;
@@ -453,8 +458,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // registers with 16-byte global stores (frees shared memory for stages).
   constexpr bool kDirectStore = (Cfg::EPI_BUFS == 0);
   static_assert(!kDirectStore || EPI == Epilogue::kStoreBF16 || EPI == Epilogue::kStoreFP16 ||
-                    EPI == Epilogue::kScaleBF16 || (EPI == Epilogue::kStoreF32 && Cfg::kRegEpi),
-                "direct stores serve the plain 16-bit epilogues and register-staged FP32 partials");
+                    EPI == Epilogue::kScaleBF16 ||
+                    (EPI == Epilogue::kStoreF32 && (Cfg::kRegEpi || Cfg::C_T)),
+                "direct stores serve the plain 16-bit epilogues and FP32 partials");
+  static_assert(!Cfg::C_T || (kDirectStore && (EPI == Epilogue::kStoreF32 ||
+                                              EPI == Epilogue::kStoreFP16)),
+                "transposed output: FP32 partials or FP16, stored from registers");
   // L2 policy hints: keep the operands resident (they are re-read by other
   // tiles), let the once-written output leave first.
   constexpr bool kHintLoads = true;
@@ -489,14 +498,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   auto ready_bar = [&](int s) { return (Cfg::SF_WARP || Cfg::kW4) ? sf_full(s) : full_bar(s); };
   // W4A16: stage s may be multiplied once its A tiles landed (full) and its
   // B rows were converted (bq_full); the MMA issuer waits on both itself
-  // (one wake-up per stage: a chain of waits through the conversion warps
-  // would add a second to every refill of the ring)
-  auto ready_probe = [&](int s, uint32_t ph) {
-    if constexpr (Cfg::kW4)
-      return ptx::mbar_test_wait(bq_full(s), ph) && ptx::mbar_test_wait(full_bar(s), ph);
-    else
-      return ptx::mbar_test_wait(ready_bar(s), ph);
-  };
+  // (a chain of waits through the conversion warps would add a second
+  // wake-up to every refill of the ring)
   auto ready_wait = [&](int s, uint32_t ph, const Watch& wt) {
     if constexpr (Cfg::kW4)
       return wait_bar(bq_full(s), ph, wt, 3) && wait_bar(full_bar(s), ph, wt, 3);
@@ -629,10 +632,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t tx =
             uint32_t(CG) * (Cfg::A_BYTES + (Cfg::kW4 ? 0 : Cfg::B_BYTES) + Cfg::SFA_BYTES +
                             uint32_t(sfb_atoms) * Cfg::SFB_ATOM_BYTES);
-        // split-K: l is the split; A and B are then single 2-D tensors (z = 0)
+        // split-K: the batch slot holds batch * k_splits + split
         const int kb_begin = sg.kb0;
         const int kb_end = sg.kb1;
-        if (p.k_splits > 1) l = 0;
+        if (p.k_splits > 1) l = l / p.k_splits;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, w, 1)) {
             ok = false;
@@ -795,58 +798,56 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = Cfg::idesc();
-      // The tensor pipe holds little more than the MMA it is executing, so
-      // thread work between a stage's last MMA and the next stage's first
-      // MMA leaves it idle, and every tcgen05 instruction costs the issuing
-      // thread tens of cycles.  The issuer walks the flat sequence of
-      // (tile, K block) jobs and keeps that gap to a few instructions: the
-      // next job (tile decode, accumulator wait, a non-blocking probe of its
-      // full barrier) is prepared between this job's MMAs; a stage is
-      // released by a commit placed after the next stage's first MMA (the
-      // commit then also waits for that MMA, which only delays the release
-      // a little); smem descriptors are stage-0 descriptors plus an offset.
+      // The tensor pipe takes the next MMA only shortly before the one it
+      // is executing ends, so whatever this thread does between a stage's
+      // last MMA and the next stage's first leaves the pipe idle.  The loop
+      // is therefore kept to: wait for the stage (already complete when the
+      // loads run ahead), fence, the stage's MMAs, the commit that releases
+      // the stage.  Measured per 4-MMA stage at 4096 x 7168 x 16384 (NVFP4,
+      // 649 cycles of MMA): 655 cycles median with this loop, 808 with an
+      // issuer that prepared the next job between the MMAs and released a
+      // stage after the next stage's first MMA (the branches around those
+      // commits and probes cost more than they saved).  Tile changes
+      // (accumulator hand-over, the next segment) stay outside the loop.
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int idx = 0;             // this cluster's segment being multiplied
-      Seg sg;
-      int pending_empty = -1;  // stage whose release commit is still to be issued
       // K tail: the last K block may need fewer than KSTEPS MMAs (the
       // zero-filled rest of its stage needs none)
       const int tail_kb = (p.K % Cfg::BK) ? p.K / Cfg::BK : -1;
       const int tail_steps = (p.K % Cfg::BK + Cfg::MMA_K - 1) / Cfg::MMA_K;
-      constexpr int kPrep = Cfg::KSTEPS > 2 ? 1 : 0;  // MMA after which the next job is prepared
-      if (seg_at<Cfg>(p, cluster_id, num_clusters, 0, sg)) {
-        int kb_begin = sg.kb0;
-        int kb_end = sg.kb1;
-        int kb = kb_begin;
-        int it = 0, acc = 0;
-        ok = wait_bar(acc_empty(0), 1u, w, 2) && ready_wait(0, 0u, w);
+      // Stage s, MMA j: start address + s * STAGE_BYTES + offset of j, i.e.
+      // the 14-bit start field (address >> 4) grows by that >> 4; shared
+      // addresses stay below 2^18 bytes, so the field never carries over.
+      const uint64_t adesc0 = ptx::sw128_kmajor_desc(stage_a(0));
+      // MN-major B: leading offset = atom stride (next 64 columns), stride
+      // offset = 8 K rows (1024 bytes)
+      const uint64_t bdesc0 = Cfg::B_MN ? ptx::smem_desc(stage_b(0), Cfg::B_ATOM_BYTES, 1024, 2)
+                                        : ptx::sw128_kmajor_desc(stage_b(0));
+      Seg sg;
+      int it = 0;
+      for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx, ++it) {
+        const int acc = it % Cfg::NUM_ACC;
+        // the accumulator's previous tile must have been read by the epilogue
+        if (!wait_bar(acc_empty(acc), (uint32_t(it / Cfg::NUM_ACC) & 1u) ^ 1u, w, 2)) {
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
-        // Stage s, MMA j: start address + s * STAGE_BYTES + offset of j, i.e.
-        // the 14-bit start field (address >> 4) grows by that >> 4; shared
-        // addresses stay below 2^18 bytes, so the field never carries over.
-        const uint64_t adesc0 = ptx::sw128_kmajor_desc(stage_a(0));
-        // MN-major B: leading offset = atom stride (next 64 columns), stride
-        // offset = 8 K rows (1024 bytes)
-        const uint64_t bdesc0 = Cfg::B_MN
-                                    ? ptx::smem_desc(stage_b(0), Cfg::B_ATOM_BYTES, 1024, 2)
-                                    : ptx::sw128_kmajor_desc(stage_b(0));
-        while (ok) {
-          const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          if (!ready_wait(stage, phase, w)) {
+            ok = false;
+            break;
+          }
+          // scales / B written by other threads' tcgen05 copies or stores:
+          // order them before the MMAs (the TMA data is ordered by the
+          // full barrier itself)
+          if constexpr (Cfg::SF_WARP || Cfg::kW4) ptx::tc_fence_after();
           const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
           const uint32_t sfa_t = sf_t0 + uint32_t(stage * Cfg::SF_COLS);
           const int nsteps = (kb == tail_kb) ? tail_steps : Cfg::KSTEPS;
-          const bool first_kb = (kb == kb_begin);
-          const bool last_kb = (kb + 1 == kb_end);
-          const int nstage = (stage + 1 == STAGES) ? 0 : stage + 1;
-          const uint32_t nphase = (stage + 1 == STAGES) ? (phase ^ 1u) : phase;
-          // the next job, filled in between this job's MMAs
-          int n_idx = idx, n_kb = kb + 1, n_kb_begin = kb_begin, n_kb_end = kb_end;
-          int n_it = it, n_acc = acc;
-          bool has_next = true, next_ready = true;
-          // (the full barrier orders the TMA data before these MMAs; no
-          // tcgen05 fence is needed per stage)
+          const bool first_kb = (kb == sg.kb0);
 #pragma unroll
           for (int j = 0; j < Cfg::KSTEPS; ++j) {
             if constexpr (!Cfg::SF_WARP) copy_scales_for(sfa_t, soff, j);
@@ -866,66 +867,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               else
                 ptx::mma_bf16<CG>(d_tmem, ad, bd, idesc, accum);
             }
-            if (j == 0 && pending_empty >= 0)
-              ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
-            if (j == kPrep) {
-              if (last_kb) {
-                Seg ns;
-                has_next = seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, ns);
-                if (has_next) {
-                  n_idx = idx + 1;
-                  n_kb_begin = ns.kb0;
-                  n_kb_end = ns.kb1;
-                  n_kb = n_kb_begin;
-                  n_it = it + 1;
-                  n_acc = n_it % Cfg::NUM_ACC;
-                  if constexpr (Cfg::NUM_ACC == 2) {
-                    // the other accumulator: its previous tile's epilogue
-                    // must have read it (independent of this tile's MMAs)
-                    ok = wait_bar(acc_empty(n_acc), (uint32_t(n_it / 2) & 1u) ^ 1u, w, 2);
-                    ptx::tc_fence_after();
-                  }
-                }
-              }
-              if (has_next) next_ready = ready_probe(nstage, nphase);
-            }
           }
-          if (last_kb) {
-            // tile done: release the stage and hand the accumulator over now
-            ptx::tc_commit<CG>(empty_bar(stage), release_mask);
-            ptx::tc_commit<CG>(acc_full(acc), pair_mask);
-            pending_empty = -1;
-          } else {
-            pending_empty = stage;
+          // release the stage to both producers once these MMAs are done
+          ptx::tc_commit<CG>(empty_bar(stage), release_mask);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          if (!has_next || !ok) break;
-          if constexpr (Cfg::NUM_ACC == 1) {
-            // a single accumulator: the epilogue of the tile just committed
-            // must have read it before the next tile's first MMA
-            if (last_kb) {
-              if (!wait_bar(acc_empty(n_acc), (uint32_t(n_it) & 1u) ^ 1u, w, 2)) {
-                ok = false;
-                break;
-              }
-              ptx::tc_fence_after();
-            }
-          }
-          if (!next_ready && !ready_wait(nstage, nphase, w)) {
-            ok = false;
-            break;
-          }
-          // scales / B written by other threads: order them before the MMAs
-          if constexpr (Cfg::SF_WARP || Cfg::kW4) ptx::tc_fence_after();
-          stage = nstage;
-          phase = nphase;
-          idx = n_idx;
-          kb = n_kb;
-          kb_begin = n_kb_begin;
-          kb_end = n_kb_end;
-          it = n_it;
-          acc = n_acc;
         }
-        if (pending_empty >= 0) ptx::tc_commit<CG>(empty_bar(pending_empty), release_mask);
+        if (!ok) break;
+        // tile done: hand the accumulator to the epilogue
+        ptx::tc_commit<CG>(acc_full(acc), pair_mask);
       }
       // Every MMA / copy issued must be complete before TMEM is released.
       ptx::tc_commit<CG>(mma_done, pair_mask);
@@ -1222,7 +1174,38 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const bool rows_live = row0 < p.M;
       const uint32_t tacc = tmem_base + lane_off + uint32_t(acc * BN + col_base);
 
-      if constexpr (Cfg::kRegEpi) {
+      if constexpr (Cfg::C_T) {
+        // Transposed output (the swapped-operand decode GEMM: D rows are the
+        // weights, D columns the activation rows): 32 columns per TMEM read;
+        // for each column, the warp's 32 lanes store 32 consecutive output
+        // elements of one activation row.  FP32 split-K partials go to
+        // [split][batch][activation row][weight], FP16 results to
+        // [batch][activation row][weight].
+        const int gi = row0 + lane;  // weight index (output column)
+        const int nbat = p.L / p.k_splits;
+        const size_t slot = (EPI == Epilogue::kStoreF32)
+                                ? size_t(l % p.k_splits) * nbat + size_t(l / p.k_splits)
+                                : size_t(l);
+#pragma unroll 1
+        for (int c = 0; c < Cfg::EPI_COLS / 32; ++c) {
+          uint32_t r0[32];
+          ptx::tmem_ld_32x32b_x32(tacc + uint32_t(32 * c), r0);
+          ptx::tmem_ld_wait_regs(r0);
+          if (c == Cfg::EPI_COLS / 32 - 1) release_acc(acc);
+          const int j0 = nb * BN + col_base + 32 * c;  // activation row of r0[0]
+          if (gi >= p.M) continue;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            if (j0 + t >= p.N) break;
+            const size_t off = (slot * p.N + size_t(j0 + t)) * size_t(p.M) + size_t(gi);
+            if constexpr (EPI == Epilogue::kStoreF32)
+              static_cast<uint32_t*>(p.c_ptr)[off] = r0[t];
+            else
+              static_cast<uint16_t*>(p.c_ptr)[off] =
+                  uint16_t(pack_f16x2(r0[t], 0u) & 0xFFFFu);
+          }
+        }
+      } else if constexpr (Cfg::kRegEpi) {
         // Read every column of this warp first, then hand the accumulator back.
         constexpr int NCH = Cfg::EPI_COLS / 64;
         uint32_t r[2 * NCH][32];
@@ -1234,10 +1217,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if constexpr (kDirectStore && EPI == Epilogue::kStoreF32) {
           // FP32 split-K partials: 32 columns per TMEM read, eight 16-byte
           // stores per lane (N % 4 == 0 keeps every piece whole)
+          // partials [split][batch][M][N]: batch slot l = batch * k_splits + split
           const int grow = row0 + lane;
+          const int nbat = p.L / p.k_splits;
+          const size_t slot = size_t(l % p.k_splits) * nbat + size_t(l / p.k_splits);
           if (grow < p.M) {
             float* dst = static_cast<float*>(p.c_ptr) +
-                         (size_t(l) * p.M + size_t(grow)) * size_t(p.N) + nb * BN + col_base;
+                         (slot * p.M + size_t(grow)) * size_t(p.N) + nb * BN + col_base;
 #pragma unroll
             for (int i = 0; i < 2 * NCH; ++i)
 #pragma unroll

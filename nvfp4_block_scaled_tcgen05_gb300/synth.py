@@ -109,9 +109,12 @@ class Nvfp4:
 
 
 NVFP4 = Nvfp4("nvfp4", 1, 4096, 7168, 16384, 1004)
-# decode-like shapes of the NVFP4 page's benchmark (M = 128), run with
-# split-K; the split count fills the SMs with (N/256) x splits CTA pairs
-# (at most 76 pairs on 152 SMs)
+# decode-like shapes of the NVFP4 page's benchmark (M = 128) and their K
+# split counts: the swapped kernel puts 256 weight rows on a CTA pair, so
+# (N / 256) x splits work units share 76 pairs: 56 units at 7168 x 16384
+# (2 splits), 64 at 4096 x 7168 (4 splits), the fastest counts measured
+# (more splits give each unit too few K blocks to amortise its start-up
+# and its transposed partial stores)
 NVFP4_DECODE = {
     "nvfp4_decode_7168x16384": (Nvfp4("nvfp4_decode_7168x16384", 1, 128, 7168, 16384, 1005), 2),
     "nvfp4_decode_4096x7168": (Nvfp4("nvfp4_decode_4096x7168", 1, 128, 4096, 7168, 1006), 4),

@@ -154,7 +154,11 @@ def test_nvfp4_splitk_rejects_bad_arguments(lib):
     big = 1 << 30
     ok = (P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P, big)
     assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 0, big, 1, 128, 256, 1024, 2, None) == 1  # NULL ws
-    assert f(*ok, 2, 128, 256, 1024, 2, None) == 2            # L != 1
+    assert f(*ok, 0, 128, 256, 1024, 2, None) == 2            # L = 0
+    # L = 2 needs twice the per-batch workspace
+    per_batch = 2 * 128 * 256 * 4
+    assert f(P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P, 2 * per_batch - 16, 2, 128, 256, 1024, 2,
+             None) == 2
     assert f(*ok, 1, 100, 256, 1024, 2, None) == 2            # M % 128
     assert f(*ok, 1, 128, 256, 1000, 2, None) == 2            # K % 256
     assert f(*ok, 1, 128, 256, 1024, 0, None) == 2            # k_splits < 1

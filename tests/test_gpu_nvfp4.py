@@ -115,10 +115,10 @@ def test_full_size_sampled(g):
 
 
 # ---------------------------------------------------------------- split-K
-def run_splitk(g, a, b, sfa, sfb, M, N, K, k_splits):
+def run_splitk(g, a, b, sfa, sfb, M, N, K, k_splits, L=1):
     c = g.gemm_nvfp4_bs_splitk(to_dev_u8(a), to_dev_u8(b), to_dev_u8(sfa), to_dev_u8(sfb),
-                               M, N, K, k_splits)
-    return bits16(c).reshape(M, N)
+                               M, N, K, k_splits, L=L)
+    return bits16(c).reshape(L * M, N)
 
 
 @pytest.mark.parametrize("M,N,K,k_splits", [(128, 256, 1024, 3), (256, 512, 2048, 5),
@@ -129,6 +129,35 @@ def test_splitk_small(g, M, N, K, k_splits):
     ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, 1, M, N, K)
     stats = check_close16(got, ref, K, MAXDQ, MAXDQ, "f16", f"nvfp4 split-K {M}x{N}x{K}/{k_splits}")
     assert stats["max_ulp"] <= 1, stats
+
+
+@pytest.mark.parametrize("L,M,N,K,k_splits", [
+    (2, 128, 512, 1024, 2),     # decode-like: operands swapped, transposed partials
+    (3, 256, 384, 2048, 3),     # swapped, two 128-row activation blocks
+    (2, 384, 256, 1024, 4),     # M > 256: the unswapped pair kernel
+])
+def test_splitk_batched(g, L, M, N, K, k_splits):
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 131 + M + L))
+    got = run_splitk(g, a, b, sfa, sfb, M, N, K, k_splits, L)
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K)
+    stats = check_close16(got, ref, K, MAXDQ, MAXDQ, "f16", f"nvfp4 split-K L={L} {M}x{N}x{K}")
+    assert stats["max_ulp"] <= 1, stats
+
+
+def test_splitk_swapped_exact_and_deterministic(g):
+    # integer-valued inputs (codes 0/1/2/3 -> e2m1 0, 0.5, 1, 1.5 with unit
+    # scales, exact sums): bit-exact against the oracle, and two runs agree
+    L, M, N, K = 1, 128, 768, 4096
+    rng = np.random.default_rng(141)
+    a = (rng.integers(0, 4, (L, M, K // 2)) | (rng.integers(0, 4, (L, M, K // 2)) << 4)).astype(np.uint8)
+    b = (rng.integers(0, 4, (L, N, K // 2)) | (rng.integers(0, 4, (L, N, K // 2)) << 4)).astype(np.uint8)
+    sfa = np.full(L * M * K // 16, UNIT, dtype=np.uint8)
+    sfb = np.full(L * N * K // 16, UNIT, dtype=np.uint8)
+    r1 = run_splitk(g, a, b, sfa, sfb, M, N, K, 5)
+    r2 = run_splitk(g, a, b, sfa, sfb, M, N, K, 5)
+    assert np.array_equal(r1, r2)
+    check_bitexact16(r1, oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K).reshape(M, N),
+                     "nvfp4 swapped split-K exact")
 
 
 def test_splitk_equals_unsplit_within_one_ulp(g):
