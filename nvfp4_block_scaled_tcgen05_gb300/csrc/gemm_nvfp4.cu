@@ -42,7 +42,14 @@
 
 namespace gb300 {
 
-using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 0, true, false>;
+// FP16 output: unreplicated A scales (6 KB less per stage), which leaves
+// room to stage the output in shared memory and write it by TMA (direct
+// 16-byte stores into 32 rows per warp instruction slowed the next tile's
+// first stages by about 5000 cycles per tile)
+using Nvfp4Pair = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 1, false, false>;
+// FP32 split-K partials (M > 256): replicated A scales, partials stored
+// straight from registers
+using Nvfp4PairPartials = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 0, true, false>;
 // Decode-like problems (M <= 256 activation rows): the operands swap roles,
 // so the weights fill the 256-row MMA M side of a CTA pair and the
 // activation rows are the MMA N = 128; the output is stored transposed.
@@ -133,8 +140,8 @@ int launch_gemm_nvfp4_splitk(const void* a, const void* b, const void* sfa, cons
       (M <= kNvfp4SwapMaxM)
           ? run_nvfp4<Nvfp4PairT, Epilogue::kStoreF32>(b, a, sfb, sfa, ws, L, N, M, K, s_eff, kbps,
                                                         dev, stream)
-          : run_nvfp4<Nvfp4Pair, Epilogue::kStoreF32>(a, b, sfa, sfb, ws, L, M, N, K, s_eff, kbps,
-                                                       dev, stream);
+          : run_nvfp4<Nvfp4PairPartials, Epilogue::kStoreF32>(a, b, sfa, sfb, ws, L, M, N, K,
+                                                               s_eff, kbps, dev, stream);
   if (rc != GEMM_OK) return rc;
   return launch_splitk_reduce_f16(ws, c, size_t(L) * M * N, s_eff, dev, stream);
 }

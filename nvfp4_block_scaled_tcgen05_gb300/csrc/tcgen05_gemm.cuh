@@ -149,9 +149,14 @@ struct TileCfg {
   static_assert(NUM_ACC == 2 || kRegEpi, "a single accumulator needs the register-staged epilogue");
   // NVFP4: dedicated warps move each stage's scale atoms into TMEM and
   // signal sf_full[stage]; the MMA thread then issues only MMAs (every
-  // tcgen05 instruction costs the issuing thread tens of cycles).  With
-  // SF_WARPS = 2 the two warps take alternate stages.
+  // tcgen05 instruction costs the issuing thread about 60 cycles).  The
+  // SF_WARPS warps share every stage: warp w copies the scales of MMAs
+  // [w * KSTEPS / SF_WARPS, (w + 1) * KSTEPS / SF_WARPS) and arrives on
+  // sf_full[stage], which expects all of them.  A stage whose TMA data lands
+  // just in time thus waits for half of its copies' issue time (6 of the 12
+  // copies with unreplicated A scales take a thread about 410 cycles).
   static constexpr int SF_WARPS = kFP4 ? 2 : 0;
+  static_assert(!kFP4 || (KSTEPS % (2 * SF_WARPS) == 0), "scale copies: whole MMA pairs per warp");
   static constexpr bool SF_WARP = SF_WARPS > 0;
   // W4A16: a producer warp of each CTA (RAW_WARP) TMA-loads its B rows'
   // packed codes (64 bytes per row per 128-deep K block) and block scales
@@ -536,7 +541,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       for (int b = 0; b < Cfg::EPI_BUFS; ++b) ptx::mbar_init(epi_bar(e, b), 1);
     ptx::mbar_init(mma_done, 1);
     if constexpr (Cfg::SF_WARP)
-      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(sf_full(s), 1);
+      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(sf_full(s), Cfg::SF_WARPS);
     if constexpr (Cfg::kW4) {
       for (int s = 0; s < STAGES; ++s) ptx::mbar_init(bq_full(s), Cfg::DQ_WARPS * CG);
       for (int q = 0; q < Cfg::RAW_STAGES; ++q) {
@@ -888,35 +893,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // Walks the same stage sequence as the MMA issuer: once a stage's TMA
     // data has landed (which also means the MMAs that last read the
     // stage's TMEM scale slot are done: the producer refilled the stage
-    // only after their release), copy its scale atoms and commit sf_full.
-    const int sfw = warp - (2 + Cfg::EPI_WARPS);  // this warp takes jobs sfw, sfw + SF_WARPS, ...
+    // only after their release), copy this warp's share of its scale atoms
+    // and commit sf_full.
+    const int sfw = warp - (2 + Cfg::EPI_WARPS);
+    constexpr int JPW = Cfg::KSTEPS / (Cfg::SF_WARPS > 0 ? Cfg::SF_WARPS : 1);  // MMAs per warp
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int last = -1;
       uint32_t last_phase = 0;
       bool ok = true;
-      int job = 0;
       Seg sg;
       for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++job) {
-          if (job % (Cfg::SF_WARPS > 0 ? Cfg::SF_WARPS : 1) == sfw) {
-            if (!wait_bar(full_bar(stage), phase, w, 6)) {
-              ok = false;
-              break;
-            }
-            // The slot's previous readers (MMAs of the MMA thread) completed
-            // before this stage could be refilled; order this thread's
-            // copies after that observed completion.
-            ptx::tc_fence_after();
-            const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
-            const uint32_t sfa_t = sf_t0 + uint32_t(stage * Cfg::SF_COLS);
-#pragma unroll
-            for (int j = 0; j < Cfg::KSTEPS; ++j) copy_scales_for(sfa_t, soff, j);
-            ptx::tc_commit<CG>(sf_full(stage), uint16_t(1u << pair_leader));
-            last = stage;
-            last_phase = phase;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          if (!wait_bar(full_bar(stage), phase, w, 6)) {
+            ok = false;
+            break;
           }
+          // The slot's previous readers (MMAs of the MMA thread) completed
+          // before this stage could be refilled; order this thread's
+          // copies after that observed completion.
+          ptx::tc_fence_after();
+          const uint64_t soff = uint64_t(uint32_t(stage) * uint32_t(Cfg::STAGE_BYTES >> 4));
+          const uint32_t sfa_t = sf_t0 + uint32_t(stage * Cfg::SF_COLS);
+#pragma unroll
+          for (int j = 0; j < JPW; ++j) copy_scales_for(sfa_t, soff, sfw * JPW + j);
+          ptx::tc_commit<CG>(sf_full(stage), uint16_t(1u << pair_leader));
+          last = stage;
+          last_phase = phase;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
