@@ -69,8 +69,15 @@ int launch_tcgen05(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
   if (clusters <= 0) clusters = std::min(p.total_tiles, cap);
   if (clusters > cap) return GEMM_ERR_LAUNCH;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   fill_launch_config<Cfg, EPI>(cfg, attr, stream);
+  // Programmatic dependent launch: the kernel's prologue (barrier set-up,
+  // TMEM allocation, tensor-map prefetch) may overlap the end of the
+  // previous kernel on the stream; every thread waits for that kernel's
+  // completion before touching global memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3(clusters * Cfg::CLUSTER);
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, tcgen05_gemm_kernel<Cfg, EPI>, ta, tb, tc, tsfa, tsfb, p);

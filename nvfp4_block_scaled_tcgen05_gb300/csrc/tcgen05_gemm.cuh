@@ -564,9 +564,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (p.sk) {
       ptx::prefetch_tmap(&tmap_sfa);  // the stream-K workspace
     }
-    // split-K / stream-K: the reduce or fixup grid may be scheduled now; it
-    // waits for this grid's end
-    if (p.sk || p.k_splits > 1) ptx::griddep_launch_dependents();
+    // The next grid on the stream (the split-K reduce, the stream-K fixup,
+    // or the next GEMM) may be scheduled now: it waits for this grid's end
+    // before it touches global memory.
+    ptx::griddep_launch_dependents();
   }
   if (warp == 1) {
     ptx::tmem_alloc<CG>(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), Cfg::TMEM_COLS);
@@ -577,6 +578,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Watch w{abort_flag, p.status, p.timeout_ns};
+  // launched as a programmatic dependent: the previous grid on the stream
+  // must be complete (and its writes visible) before any global access
+  ptx::griddep_wait();
 
   // NVFP4: the scale atoms of MMA j of stage s go into the stage's TMEM
   // slot (issued by the scale warp, which then commits sf_full[s]).
