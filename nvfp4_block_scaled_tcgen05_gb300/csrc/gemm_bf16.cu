@@ -28,6 +28,12 @@ using Bf16SingleNN = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2, true, false, 1, tr
 // 8 epilogue warps (each 128 of the 256 columns, 4 output buffers) keep more
 // of that stream in flight than 4 (measured 75.9 -> 68.9 us at 4096 x 17408)
 using Bf16PairStream = TileCfg<Operand::kBF16, 2, 256, 3, 8, 4>;
+// K <= 64 (one K block per tile, e.g. LoRA rank 16): one operand stage is
+// enough (a tile's single MMA takes ~160 cycles against microseconds of
+// output streaming), and the freed 64 KB hold a third set of output boxes,
+// so each warp requests the old output two tiles ahead
+using Bf16PairStreamK1 = TileCfg<Operand::kBF16, 2, 256, 1, 8, 6>;
+constexpr int kStreamK1MaxK = 64;
 using Bf16SingleStream = TileCfg<Operand::kBF16, 1, 256, 2, 4, 8>;
 constexpr int kStreamMaxK = 256;  // scaled-acc K up to this uses the streaming configurations
 
@@ -349,9 +355,12 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   const long long pair_tiles = (long long)((M + 255) / 256) * ((N + 255) / 256);
   int cg = (pair_tiles >= dev.num_sms / 2) ? 2 : 1;
   if (const int o = cta_group_override()) cg = o;
-  if (scaled_acc && K <= kStreamMaxK)
+  if (scaled_acc && K <= kStreamMaxK) {
+    if (cg == 2 && K <= kStreamK1MaxK)
+      return run_bf16<Bf16PairStreamK1>(A, B, C, M, N, K, scale, true, dev, stream);
     return cg == 2 ? run_bf16<Bf16PairStream>(A, B, C, M, N, K, scale, true, dev, stream)
                    : run_bf16<Bf16SingleStream>(A, B, C, M, N, K, scale, true, dev, stream);
+  }
   // Plain outputs: a CTA pair covers 256 rows with the same per-SM work as
   // one CTA on 128 rows, so pairs (128-deep stages, half the B traffic per
   // SM) occupy as many SMs as single CTAs whenever M spans two row blocks.

@@ -53,7 +53,7 @@ using Nvfp4PairPartials = TileCfg<Operand::kNVFP4, 2, 256, 5, 8, 0, true, false>
 // Decode-like problems (M <= 256 activation rows): the operands swap roles,
 // so the weights fill the 256-row MMA M side of a CTA pair and the
 // activation rows are the MMA N = 128; the output is stored transposed.
-using Nvfp4PairT = TileCfg<Operand::kNVFP4, 2, 128, 6, 4, 0, true, false, 1, false, true>;
+using Nvfp4PairT = TileCfg<Operand::kNVFP4, 2, 128, 6, 4, 1, true, false, 1, false, true>;
 
 // `out` is the FP16 output (EPI = kStoreFP16) or, with splits > 1 (L = 1),
 // the FP32 workspace [splits][M][N] (EPI = kStoreF32).
@@ -70,9 +70,20 @@ static int run_nvfp4(const void* a, const void* b, const void* sfa, const void* 
   if (rc == GEMM_OK)
     rc = encode_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, kb, uint64_t(N), uint64_t(L), 128,
                         Cfg::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc == GEMM_OK)
-    rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c, uint64_t(N), uint64_t(M),
-                        uint64_t(L), 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == GEMM_OK) {
+    if constexpr (Cfg::C_T) {
+      // transposed output [slot][N][M] (M = the weights, innermost), 32 x 32
+      // boxes; slot = batch, or split * L + batch for FP32 partials
+      const bool f32 = (EPI == Epilogue::kStoreF32);
+      rc = encode_tmap_3d(&tc, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          f32 ? 4 : 2, c, uint64_t(M), uint64_t(N),
+                          uint64_t(splits > 1 ? splits * L : L), 32, 32,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      rc = encode_tmap_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c, uint64_t(N), uint64_t(M),
+                          uint64_t(L), 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+  }
   // scales: one row of rest_k * 512 bytes (= rest_k * 64 u64) per (l, 128-row block)
   if (rc == GEMM_OK) {
     if constexpr (Cfg::SFA_REP) {

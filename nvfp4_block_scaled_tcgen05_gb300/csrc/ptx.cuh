@@ -163,17 +163,13 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// The same arrive with the default (CTA-scope release) semantics, the form
-// cluster pipelines use for a consumer's per-stage signal to the other CTA
-// of a pair.  Measured on GB300: the cluster-scope release above costs the
-// issuing warp long enough that, issued every pipeline stage, it stalls the
-// pipeline; this form does not.
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of
+// the cluster), with the default (CTA-scope release) semantics, the form
+// cluster pipelines use for a consumer's signal to the other CTA of a pair
+// (a converted stage, a drained accumulator).  Measured on GB300: a
+// cluster-scope release (.release.cluster) costs the issuing warp long
+// enough (it waits for the warp's bulk stores in flight) that, issued
+// every pipeline stage or tile, it stalls the pipeline; this form does not.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }

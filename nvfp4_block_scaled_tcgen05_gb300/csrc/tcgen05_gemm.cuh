@@ -140,8 +140,7 @@ struct TileCfg {
   static_assert(KSUB == 1 || (KSUB == 2 && !kFP4), "K sub-tiles: BF16 only");
   static_assert(!B_MN || (!kFP4 && B_ROWS % 64 == 0), "MN-major B: BF16 operands");
   static constexpr int B_ATOM_BYTES = 64 * KSUB * 128;  // one 64-column MN-major atom of a stage
-  // the MMA issuer releases a stage only after the next stage's first MMA
-  static_assert(STAGES >= 2, "at least two pipeline stages");
+  static_assert(STAGES >= 1, "pipeline stages");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA");
   static_assert(!kFP4 || BN % 128 == 0, "NVFP4 BN must cover whole 128-row scale atoms");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
@@ -456,9 +455,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   constexpr int BN = Cfg::BN;
   constexpr int CG = Cfg::CG;
   constexpr bool kFP4 = Cfg::kFP4;
-  // scaled-acc with two buffer halves per epilogue warp: prefetch the next tile
+  // Scaled-acc with LA_SETS >= 2 sets of output boxes per epilogue warp (one
+  // tile's boxes each): the old output of the next LA_SETS - 1 tiles is
+  // requested before this tile's accumulator is awaited.
+  constexpr int LA_NCH = Cfg::EPI_COLS / 64;  // 64-column boxes per warp and tile
+  constexpr int LA_SETS = Cfg::EPI_BUFS / LA_NCH;
   constexpr bool kLookahead = (EPI == Epilogue::kScaledAccBF16) && !Cfg::kRegEpi &&
-                              (Cfg::EPI_BUFS == 2 * (Cfg::EPI_COLS / 64));
+                              (Cfg::EPI_BUFS % LA_NCH == 0) && (LA_SETS >= 2);
   // Without epilogue buffers the 16-bit outputs are written straight from
   // registers with 16-byte global stores (frees shared memory for stages).
   constexpr bool kDirectStore = (Cfg::EPI_BUFS == 0);
@@ -466,9 +469,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     EPI == Epilogue::kScaleBF16 ||
                     (EPI == Epilogue::kStoreF32 && (Cfg::kRegEpi || Cfg::C_T)),
                 "direct stores serve the plain 16-bit epilogues and FP32 partials");
-  static_assert(!Cfg::C_T || (kDirectStore && (EPI == Epilogue::kStoreF32 ||
-                                              EPI == Epilogue::kStoreFP16)),
-                "transposed output: FP32 partials or FP16, stored from registers");
+  static_assert(!Cfg::C_T || EPI == Epilogue::kStoreF32 || EPI == Epilogue::kStoreFP16,
+                "transposed output: FP32 partials or FP16");
+  static_assert(!Cfg::C_T || kDirectStore || Cfg::EPI_BUFS == 1,
+                "transposed output through shared memory: one 32 x 32 box per warp");
   // L2 policy hints: keep the operands resident (they are re-read by other
   // tiles), let the once-written output leave first.
   constexpr bool kHintLoads = true;
@@ -1128,18 +1132,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint32_t epi_pending = 0;    // bit b: a load into buffer b has not been waited for
     bool ok = true;
     int it = 0;
+    // The warp's TMEM reads of the accumulator are complete (waited for);
+    // hand it back to the MMA issuer.  The arrive on the leader's barrier
+    // uses the default (CTA-scope) release: the cluster-scope form waited
+    // for this warp's TMA output stores still in flight and cost the
+    // scaled-acc epilogue about 2500 cycles per tile.
     auto release_acc = [&](int acc) {
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (CG == 2) ptx::mbar_arrive_cluster(acc == 0 ? ae_leader0 : ae_leader1);
+        if constexpr (CG == 2) ptx::mbar_arrive_remote(acc == 0 ? ae_leader0 : ae_leader1);
         else ptx::mbar_arrive(acc_empty(acc));
       }
     };
-    // Look-ahead loads of the old output boxes of tile `t` into buffer half `half`.
-    auto prefetch_out = [&](const Seg& s2, int half) {
+    // Look-ahead loads of the old output boxes of segment s2's tile into box set `set`.
+    auto prefetch_out = [&](const Seg& s2, int set) {
       if constexpr (kLookahead) {
-        constexpr int NCH = Cfg::EPI_COLS / 64;
+        constexpr int NCH = LA_NCH;
         int l2, mb2, nb2;
         decode_tile<Cfg>(s2.tile, p, l2, mb2, nb2);
         const int r0 = mb2 * Cfg::TILE_M + int(peer) * Cfg::BM + q * 32;
@@ -1148,7 +1157,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int c = 0; c < NCH; ++c) {
           const int col0 = nb2 * BN + col_base + c * 64;
           if (col0 >= p.N) continue;
-          const int b = half * NCH + c;
+          const int b = set * NCH + c;
           if (lane == 0) {
             ptx::mbar_arrive_expect_tx(epi_bar(e, b), Cfg::EPI_BOX_BYTES);
             ptx::tma_load_3d(buf0 + b * Cfg::EPI_BOX_BYTES, &tmap_c, epi_bar(e, b), col0, r0, l2);
@@ -1159,7 +1168,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     };
     Seg sg;
     if constexpr (kLookahead) {
-      if (seg_at<Cfg>(p, cluster_id, num_clusters, 0, sg)) prefetch_out(sg, 0);
+      for (int k = 0; k < LA_SETS - 1; ++k)
+        if (seg_at<Cfg>(p, cluster_id, num_clusters, k, sg)) prefetch_out(sg, k);
     }
     for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx, ++it) {
       int l, mb, nb;
@@ -1168,11 +1178,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint32_t acc_phase = uint32_t(it / Cfg::NUM_ACC) & 1u;
       if constexpr (kLookahead) {
         Seg ns;
-        if (seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, ns)) {
-          // the stores of the previous tile read the other buffer half
+        if (seg_at<Cfg>(p, cluster_id, num_clusters, idx + LA_SETS - 1, ns)) {
+          // that tile's set last held the previous tile's boxes: their
+          // stores must have read them
           if (lane == 0) ptx::bulk_wait_group_read<0>();
           __syncwarp();
-          prefetch_out(ns, (it + 1) & 1);
+          prefetch_out(ns, (it + LA_SETS - 1) % LA_SETS);
         }
       }
       ok = __all_sync(0xffffffffu, wait_bar(acc_full(acc), acc_phase, w, 4));
@@ -1184,33 +1195,68 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
       if constexpr (Cfg::C_T) {
         // Transposed output (the swapped-operand decode GEMM: D rows are the
-        // weights, D columns the activation rows): 32 columns per TMEM read;
-        // for each column, the warp's 32 lanes store 32 consecutive output
-        // elements of one activation row.  FP32 split-K partials go to
-        // [split][batch][activation row][weight], FP16 results to
-        // [batch][activation row][weight].
+        // weights, D columns the activation rows), 32 columns per TMEM read.
+        // FP32 split-K partials go to [split][batch][activation row][weight],
+        // FP16 results to [batch][activation row][weight].
         const int gi = row0 + lane;  // weight index (output column)
         const int nbat = p.L / p.k_splits;
         const size_t slot = (EPI == Epilogue::kStoreF32)
                                 ? size_t(l % p.k_splits) * nbat + size_t(l / p.k_splits)
                                 : size_t(l);
+        if constexpr (kDirectStore) {
+          // for each column, the warp's 32 lanes store 32 consecutive
+          // output elements of one activation row
 #pragma unroll 1
-        for (int c = 0; c < Cfg::EPI_COLS / 32; ++c) {
-          uint32_t r0[32];
-          ptx::tmem_ld_32x32b_x32(tacc + uint32_t(32 * c), r0);
-          ptx::tmem_ld_wait_regs(r0);
-          if (c == Cfg::EPI_COLS / 32 - 1) release_acc(acc);
-          const int j0 = nb * BN + col_base + 32 * c;  // activation row of r0[0]
-          if (gi >= p.M) continue;
+          for (int c = 0; c < Cfg::EPI_COLS / 32; ++c) {
+            uint32_t r0[32];
+            ptx::tmem_ld_32x32b_x32(tacc + uint32_t(32 * c), r0);
+            ptx::tmem_ld_wait_regs(r0);
+            if (c == Cfg::EPI_COLS / 32 - 1) release_acc(acc);
+            const int j0 = nb * BN + col_base + 32 * c;  // activation row of r0[0]
+            if (gi >= p.M) continue;
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            if (j0 + t >= p.N) break;
-            const size_t off = (slot * p.N + size_t(j0 + t)) * size_t(p.M) + size_t(gi);
-            if constexpr (EPI == Epilogue::kStoreF32)
-              static_cast<uint32_t*>(p.c_ptr)[off] = r0[t];
-            else
-              static_cast<uint16_t*>(p.c_ptr)[off] =
-                  uint16_t(pack_f16x2(r0[t], 0u) & 0xFFFFu);
+            for (int t = 0; t < 32; ++t) {
+              if (j0 + t >= p.N) break;
+              const size_t off = (slot * p.N + size_t(j0 + t)) * size_t(p.M) + size_t(gi);
+              if constexpr (EPI == Epilogue::kStoreF32)
+                static_cast<uint32_t*>(p.c_ptr)[off] = r0[t];
+              else
+                static_cast<uint16_t*>(p.c_ptr)[off] =
+                    uint16_t(pack_f16x2(r0[t], 0u) & 0xFFFFu);
+            }
+          }
+        } else {
+          // Through this warp's box in shared memory, [32 activation rows]
+          // [32 weights] (row t: the warp's 32 weights for activation row
+          // j0 + t; lane = weight, so each row is written conflict-free),
+          // then one TMA store per 32 columns; the tensor map clips rows
+          // and weights past the output.  Scattered 4-byte stores of the
+          // same data took about 4 us per 128 x 128 tile.
+          uint8_t* box = smem + (buf0 - sbase);
+#pragma unroll 1
+          for (int c = 0; c < Cfg::EPI_COLS / 32; ++c) {
+            uint32_t r0[32];
+            ptx::tmem_ld_32x32b_x32(tacc + uint32_t(32 * c), r0);
+            ptx::tmem_ld_wait_regs(r0);
+            if (c == Cfg::EPI_COLS / 32 - 1) release_acc(acc);
+            const int j0 = nb * BN + col_base + 32 * c;  // activation row of r0[0]
+            if (!rows_live || j0 >= p.N) continue;       // warp-uniform
+            if (lane == 0) ptx::bulk_wait_group_read<0>();  // the box's previous store read it
+            __syncwarp();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              if constexpr (EPI == Epilogue::kStoreF32)
+                reinterpret_cast<uint32_t*>(box)[t * 32 + lane] = r0[t];
+              else
+                reinterpret_cast<uint16_t*>(box)[t * 32 + lane] =
+                    uint16_t(pack_f16x2(r0[t], 0u) & 0xFFFFu);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&tmap_c, buf0, row0, j0, int(slot));
+              ptx::bulk_commit_group();
+            }
           }
         }
       } else if constexpr (Cfg::kRegEpi) {
@@ -1275,15 +1321,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
         }
       } else if constexpr (kLookahead) {
-        // Scaled-acc with look-ahead: the old output boxes of the next tile
-        // were (or are now) requested before this tile's accumulator is
-        // awaited, so HBM reads overlap the MMA and this tile's stores.
-        constexpr int NCH = Cfg::EPI_COLS / 64;
-        const int half = it & 1;
-        (void)half;
+        // Scaled-acc with look-ahead: the old output boxes of this tile were
+        // requested LA_SETS - 1 tiles ago, so HBM reads overlap the MMAs and
+        // the stores of the tiles in between.
+        constexpr int NCH = LA_NCH;
+        const int set = it % LA_SETS;
 #pragma unroll 1
         for (int c = 0; c < NCH; ++c) {
-          const int b = half * NCH + c;
+          const int b = set * NCH + c;
           const uint32_t sbuf = buf0 + b * Cfg::EPI_BOX_BYTES;
           const int col0 = nb * BN + col_base + c * 64;
           const bool live = rows_live && col0 < p.N;
