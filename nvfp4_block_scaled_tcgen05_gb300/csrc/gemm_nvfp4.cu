@@ -8,36 +8,36 @@
 // which tcgen05.cp moves into a per-stage TMEM slot before the stage's 4
 // MMAs.  The MMA reads the scales of row 32*i + g from TMEM lane 32*i + g,
 // column base + i, so an atom has to land in all four 32-lane quarters:
-//   * A scales are staged four times in shared memory (one TMA box whose
-//     replica dimension has stride 0), so one 128-lane x 32-byte copy fills
-//     the scale columns of two MMAs (2 copies per stage);
-//   * B scales (the two atoms of a 256-row B tile) are staged once and
-//     copied with the replicating 32x128b.warpx4 shape (8 copies per stage),
-//     which reads 4x fewer shared-memory bytes than staging them replicated.
-// A dedicated warp issues the copies and signals the MMA thread through a
-// per-stage barrier, so the MMA thread issues only MMAs.  Measured at
-// 4096 x 7168 x 16384 on GB300: 228 us with both scale sets replicated and
-// copied by the MMA thread, 191 us with this arrangement and 5 stages.
+// the 32x128b.warpx4 copy replicates one atom into them (12 copies per
+// stage for a 256-row B tile).  The FP32-partial and decode configurations
+// instead stage the A atoms four times in shared memory (one TMA box whose
+// replica dimension has stride 0), so that one 128-lane x 32-byte copy
+// fills the scale columns of two MMAs.  Two dedicated warps share every
+// stage's copies (MMAs 0-1 and 2-3) and both arrive on the stage's barrier,
+// so the MMA thread issues only MMAs and a stage whose data lands just in
+// time waits for half of the copies' issue time (each tcgen05 instruction
+// costs the issuing thread about 60 cycles).
 // One TMEM accumulator (256 columns) plus the scale slots fill the 512
 // columns, so the epilogue is register-staged: 8 warps read the whole
-// accumulator, release it, then convert and store straight to global
-// memory while the next tile's MMAs run.
+// accumulator, release it, then convert it into per-warp boxes in shared
+// memory that TMA writes out, while the next tile's MMAs run.
 //
 // Configuration: CTA pairs (cta_group::2, 256 x 256 tiles, each CTA stages
 // its 128 A rows, 128 B rows and the scales of all 256 B rows, 5 stages)
-// for every shape; with M = 128 the second CTA's rows lie past M (its loads
-// are zero-filled, its stores skipped).  A single-CTA configuration
-// (cta_group::1, 128 x 256 tiles, 3 stages, scale-copy warps) faulted the
-// GPU twice when launched back to back; the cause was not found, so it is
-// not used.
+// for every shape with M > 256; with M = 128 the second CTA's rows would lie
+// past M, so decode-like problems swap the operands (below).  A single-CTA
+// configuration (cta_group::1, 128 x 256 tiles, 3 stages, scale-copy warps)
+// faulted the GPU twice when launched back to back; the cause was not
+// found, so it is not used.
 // Split-K (decode-like M = 128 with few output tiles): FP32 partials of
-// K-block chunks go straight from registers into a caller workspace, then an
-// ordered reduce rounds once to FP16 ("gemm_dense.rs", dense_gemm_splitk,
-// applied to the block-scaled GEMM).  With M <= 256 the operands swap roles
-// (D = B . A^T, the weights on the 256-row MMA side of the CTA pair, the
-// activation rows as MMA N = 128) and the epilogue stores D transposed: no
-// MMA rows are spent on zero fill, and the 256-row weight tiles times the
-// splits give enough work units for every CTA pair.
+// K-block chunks go into a caller workspace, then an ordered reduce rounds
+// once to FP16 ("gemm_dense.rs", dense_gemm_splitk, applied to the
+// block-scaled GEMM).  With M <= 256 the operands swap roles (D = B . A^T,
+// the weights on the 256-row MMA side of the CTA pair, the activation rows
+// as MMA N = 128) and the epilogue writes D transposed, one 32 x 32 FP32
+// box per warp by TMA: no MMA rows are spent on zero fill, and the
+// 256-row weight tiles times the splits give enough work units for the
+// CTA pairs.
 #include "launch.cuh"
 
 namespace gb300 {
