@@ -297,7 +297,8 @@ def tensor_rate(torch, dev, local, n_mma=8192):
              (1, 256, 0, 0, 4, 0), (1, 256, 0, 0, 64, 0), (1, 256, 0, 0, 4096, 0),
              (1, 256, 0, 0, 4, 64), (1, 256, 0, 0, 4, 128), (1, 256, 0, 0, 4, 65),
              (1, 256, 0, 0, 4, 129), (1, 256, 8, 0, 4, 129), (0, 256, 0, 0, 4, 64),
-             (0, 128, 0, 0, 0, 0), (1, 128, 0, 0, 0, 0), (1, 128, 4, 2, 0, 0),
+             (0, 192, 0, 0, 0, 0), (0, 192, 0, 0, 4, 64), (0, 128, 0, 0, 0, 0),
+             (1, 128, 0, 0, 0, 0), (1, 128, 4, 2, 0, 0),
              (1, 128, 4, 2, 4, 64), (1, 128, 4, 2, 4, 129))
     for kind, mma_n, copies, wide, commit_every, flags in cases:
         flops = 2.0 * 256 * mma_n * kdepth[kind]

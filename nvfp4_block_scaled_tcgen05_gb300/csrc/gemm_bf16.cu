@@ -21,6 +21,9 @@ using Bf16Pair = TileCfg<Operand::kBF16, 2, 256, 6, 4, 2>;
 using Bf16Single = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2>;
 // plain BF16 output: 128-deep stages (8 MMAs per stage), 3 stages
 using Bf16PairStore = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 2>;
+// the same with 192-column tiles, for shapes whose 256-column tiles leave
+// much of the last round of CTA pairs idle (see pair_tile_n)
+using Bf16PairStore192 = TileCfg<Operand::kBF16, 2, 192, 3, 4, 2, true, false, 2>;
 // NN layout (B stored [K][N]): the same tiles with B staged MN-major
 using Bf16PairStoreNN = TileCfg<Operand::kBF16, 2, 256, 3, 4, 2, true, false, 2, true>;
 using Bf16SingleNN = TileCfg<Operand::kBF16, 1, 256, 4, 4, 2, true, false, 1, true>;
@@ -350,6 +353,26 @@ int launch_gemm_bf16_nn(const void* A, const void* B, void* C, int M, int N, int
                  : run_bf16<Bf16SingleNN>(A, B, C, M, N, K, 0.0f, false, dev, stream);
 }
 
+// Column width of the plain-output pair tiles: 256 or 192, whichever gives
+// the shorter critical path = rounds of tiles over the CTA pairs x cycles of
+// one pair MMA at that width (measured: 162.3 cycles for 256x256x16, 130.3
+// for 256x192x16; bench.py --tensor-rate).  192-column tiles re-read A
+// more, but on shapes whose 256-wide tiles fill the pairs badly they win:
+// 5120x512x2048 16.3 -> 13.9 us (60 tiles instead of 40 on 76 pairs),
+// 5120x2048x2048 34.7 -> 31.4 us and 5120x2048x11008 158.9 -> 142.9 us
+// (220 tiles in 3 rounds instead of 160 in 3); gate/up (860 vs 1160
+// tiles) stays at 256.  Results are the same at either width (the K loop
+// of every output is the same).
+static int pair_tile_n(int M, int N, const DeviceInfo& dev) {
+  const long long pairs = dev.num_sms / 2;
+  const long long mb = (M + 255) / 256;
+  auto path = [&](int bn, double mma_cycles) {
+    const long long tiles = mb * ((N + bn - 1) / bn);
+    return double((tiles + pairs - 1) / pairs) * mma_cycles;
+  };
+  return path(192, 130.3) < path(256, 162.3) ? 192 : 256;
+}
+
 int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float scale,
                      bool scaled_acc, const DeviceInfo& dev, cudaStream_t stream) {
   const long long pair_tiles = (long long)((M + 255) / 256) * ((N + 255) / 256);
@@ -366,7 +389,9 @@ int launch_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K,
   // SM) occupy as many SMs as single CTAs whenever M spans two row blocks.
   if (!scaled_acc && !cta_group_override()) cg = (M > 128) ? 2 : 1;
   if (!scaled_acc && cg == 2)
-    return run_bf16<Bf16PairStore>(A, B, C, M, N, K, 0.0f, false, dev, stream);
+    return pair_tile_n(M, N, dev) == 192
+               ? run_bf16<Bf16PairStore192>(A, B, C, M, N, K, 0.0f, false, dev, stream)
+               : run_bf16<Bf16PairStore>(A, B, C, M, N, K, 0.0f, false, dev, stream);
   return cg == 2 ? run_bf16<Bf16Pair>(A, B, C, M, N, K, scale, scaled_acc, dev, stream)
                  : run_bf16<Bf16Single>(A, B, C, M, N, K, scale, scaled_acc, dev, stream);
 }

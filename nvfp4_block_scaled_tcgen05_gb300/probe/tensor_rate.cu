@@ -6,8 +6,9 @@
 //   kind 0: tcgen05.mma.cta_group::2.kind::f16 (BF16), 256 x N x 16
 //   kind 1: tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X,
 //           256 x N x 64
-// with N = 256 (the square tiles) or 128 (the decode tiles, whose N is the
-// activation rows).
+// with N = 256 (the square tiles), 192 (the narrower BF16 tiles of
+// under-filled shapes) or 128 (the decode tiles, whose N is the activation
+// rows).
 //
 // Each CTA pair zeroes 64 KB of shared memory (the operands: every MMA reads
 // the same zero tiles, so only the issue and execution rate is measured, not
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(128, 1)
 extern "C" __attribute__((visibility("default"))) int probe_tensor_rate(
     int kind, int mma_n, int clusters, int n_mma, int copies, int wide, int commit_every,
     int flags, unsigned long long* out, void* stream) {
-  if (kind < 0 || kind > 1 || (mma_n != 128 && mma_n != 256) || clusters < 1 ||
+  if (kind < 0 || kind > 1 || (mma_n != 128 && mma_n != 192 && mma_n != 256) || clusters < 1 ||
       clusters > 1024 || n_mma < 4 || n_mma % 4 || copies < 0 || copies > 64 || copies % 2 ||
       wide < 0 || wide > 16 || wide % 2 || commit_every < 0 || commit_every > 8192 || flags < 0 || flags > 255 ||
       (flags & 64 && flags & 128) || !out)
