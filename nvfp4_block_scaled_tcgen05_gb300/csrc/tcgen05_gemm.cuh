@@ -123,7 +123,11 @@ struct TileCfg {
   static constexpr int SFB_ATOM_BYTES = kFP4 ? KSTEPS * SF_ATOM * (SFB_REP ? 4 : 1) : 0;  // per B atom
   static constexpr int SFB_BYTES = SFB_ATOMS * SFB_ATOM_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int EPI_BOX_BYTES = 32 * 128;  // 32 rows x 64 16-bit values
+  // Output boxes: 32 rows x 64 16-bit values, or 16 rows for W4A16, whose
+  // stages and code ring leave room for only 8 KB of boxes (its warps then
+  // write their 32 rows as two boxes)
+  static constexpr int EPI_BOX_ROWS = kW4 ? 16 : 32;
+  static constexpr int EPI_BOX_BYTES = EPI_BOX_ROWS * 128;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BOX_BYTES;  // 0: direct stores
   // TMEM columns: accumulators first, then one scale slot per smem stage.
   static constexpr int SF_COLS = kFP4 ? KSTEPS * 4 * (1 + SFB_ATOMS) : 0;
@@ -174,7 +178,7 @@ struct TileCfg {
   static constexpr bool kW4T = kW4 && B_MN;
   static constexpr int DQ_WARPS = kW4 ? 8 : 0;
   static constexpr int DQ_ROWS = kW4 ? B_ROWS / DQ_WARPS : 0;
-  static constexpr int RAW_STAGES = kW4 ? 3 : 0;
+  static constexpr int RAW_STAGES = kW4 ? 2 : 0;
   static constexpr int RAW_CODE_BYTES = kW4 ? B_ROWS * 64 : 0;  // codes of a job
   static constexpr int RAW_BYTES = kW4 ? B_ROWS * (64 + 16) : 0;  // + the scale pairs
   static constexpr int RAW_TX_BYTES = kW4T ? B_ROWS * (64 + 8) : RAW_BYTES;  // bytes a job loads
@@ -1416,6 +1420,44 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               for (int e = 0; e < 8; ++e)
                 if (col0 + 8 * j + e < p.N)
                   dst[8 * j + e] = uint16_t(ow[e >> 1] >> (16 * (e & 1)));
+            }
+          }
+        }
+      } else if constexpr (Cfg::EPI_BOX_ROWS < 32) {
+        // Boxes of EPI_BOX_ROWS rows: per 64 columns, the warp's 32 rows go
+        // out as 32 / EPI_BOX_ROWS boxes, each written by its lanes and
+        // stored by TMA (boxes that start past row M are skipped; the map
+        // clips the rest).
+        static_assert(EPI == Epilogue::kScaleBF16 || EPI == Epilogue::kStoreBF16,
+                      "short boxes: plain 16-bit outputs");
+        constexpr int HB = 32 / Cfg::EPI_BOX_ROWS;
+#pragma unroll 1
+        for (int c = 0; c < Cfg::EPI_COLS / 64; ++c) {
+          const int col0 = nb * BN + col_base + c * 64;
+          uint32_t r0[32], r1[32];
+          const uint32_t taddr = tacc + uint32_t(c * 64);
+          ptx::tmem_ld_32x32b_x32(taddr, r0);
+          ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
+          ptx::tmem_ld_wait_regs(r0);
+          ptx::tmem_ld_wait_regs(r1);
+          if (c == Cfg::EPI_COLS / 64 - 1) release_acc(acc);
+          if (!(rows_live && col0 < p.N)) continue;
+#pragma unroll 1
+          for (int h = 0; h < HB; ++h) {
+            if (row0 + h * Cfg::EPI_BOX_ROWS >= p.M) break;  // warp-uniform
+            const uint32_t sbuf = buf0 + int(chunk_ctr % Cfg::EPI_BUFS) * Cfg::EPI_BOX_BYTES;
+            ++chunk_ctr;
+            // The TMA store that last read this buffer must be done with it.
+            if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
+            __syncwarp();
+            if (lane / Cfg::EPI_BOX_ROWS == h)
+              write_box_row<EPI>(smem + (sbuf - sbase) + (lane % Cfg::EPI_BOX_ROWS) * 128, lane,
+                                 r0, r1, p.scale);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              store_box(sbuf, col0, row0 + h * Cfg::EPI_BOX_ROWS, l);
+              ptx::bulk_commit_group();
             }
           }
         }
