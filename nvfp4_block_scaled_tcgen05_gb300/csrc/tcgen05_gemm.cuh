@@ -946,12 +946,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ W4A16 weights
     // Warp d owns DQ_ROWS weight rows of this CTA's half of the tile and
     // walks the same job sequence as the producers.  Per job: wait for its
-    // codes and scales in the raw ring, read this warp's rows into registers
-    // and hand the slot back, wait until the MMAs that last read the B stage
-    // are done, write the BF16 weights in the MMA's 128-byte-swizzled K-major
-    // layout, make the writes visible to the tensor core (async proxy) and
-    // arrive on the leader CTA's bq_full (the MMA issuer also waits for the
-    // stage's A tiles on full).
+    // codes and scales in the raw ring, read this warp's rows into registers,
+    // wait until the MMAs that last read the B stage are done, write the
+    // BF16 weights in the MMA's 128-byte-swizzled K-major layout, then one
+    // fence (async proxy) orders both the raw reads and the B writes, and the
+    // warp hands the raw slot back and arrives on the leader CTA's bq_full
+    // (the MMA issuer also waits for the stage's A tiles on full).  Per job
+    // a conversion warp measured ~730 cycles converting and ~250 in each
+    // fence-and-signal, against 1298 cycles of MMA per stage, so the second
+    // fence a separate early release of the raw slot needed cost more than
+    // the release gained (1016 x 12288 x 2048: 49.9 -> 48.6 us).
     // Lanes: row prow (lane / 4) of an 8-row pass, K quarter kq (lane % 4).
     // The lanes of quarters 2 and 3 convert their two 16-element halves in
     // swapped order, which staggers the 16-byte chunks written together by
@@ -991,12 +995,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             scl[ps] = *reinterpret_cast<const uint4*>(slot + Cfg::RAW_CODE_BYTES +
                                                       (kk >> 3) * Cfg::B_ROWS + cq * 16);
           }
-          // The slot is refilled by TMA (the async proxy): order these
-          // generic reads before that write.  Without the fence a load still
-          // in flight at the release can return the next job's bytes.
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(raw_empty(q));
+          // The slot is released after the B writes below, behind the same
+          // fence: it is refilled by TMA (the async proxy), which must not
+          // overtake these generic reads (without a fence a load still in
+          // flight at the release can return the next job's bytes).
+          const int q_read = q;
           if (++q == Cfg::RAW_STAGES) {
             q = 0;
             qphase ^= 1u;
@@ -1029,9 +1032,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               }
             }
           }
+          // one fence orders the raw slot's generic reads (before its TMA
+          // refill) and the B writes (before the tensor core reads them)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
+            ptx::mbar_arrive(raw_empty(q_read));
             if constexpr (CG == 2) ptx::mbar_arrive_remote(bq_target + 8 * stage);
             else ptx::mbar_arrive(bq_full(stage));
           }
@@ -1074,10 +1080,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           codes[ps] = c;
           scl[ps] = sv;
         }
-        // generic reads of a slot that TMA refills: fence before the release
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(raw_empty(q));
+        // generic reads of a slot that TMA refills: released after the B
+        // writes, behind the same fence
+        const int q_read = q;
         if (++q == Cfg::RAW_STAGES) {
           q = 0;
           qphase ^= 1u;
@@ -1100,9 +1105,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
+        // one fence orders the raw slot's generic reads (before its TMA
+        // refill) and the B writes (before the tensor core reads them)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+          ptx::mbar_arrive(raw_empty(q_read));
           if constexpr (CG == 2) ptx::mbar_arrive_remote(bq_target + 8 * stage);
           else ptx::mbar_arrive(bq_full(stage));
         }
