@@ -1546,7 +1546,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // Loads that were issued but never waited for (abort path) must land.
       for (int b = 0; b < Cfg::EPI_BUFS; ++b)
         if (epi_pending & (1u << b)) drain_bar(epi_bar(e, b), (epi_parity >> b) & 1u, w);
-      ptx::bulk_wait_group<0>();
+      // The stores must have read their boxes before the shared memory is
+      // released; their writes complete with the grid (a dependent launch
+      // sees them after its griddepcontrol.wait), so the CTA does not wait
+      // for them.
+      ptx::bulk_wait_group_read<0>();
     }
     __syncwarp();
   }
