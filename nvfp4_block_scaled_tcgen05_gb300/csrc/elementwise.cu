@@ -52,7 +52,10 @@ __global__ void __launch_bounds__(kThreads)
     splitk_reduce_kernel(const float* __restrict__ ws, uint16_t* __restrict__ C, size_t n,
                          int splits) {
   // launched as a programmatic dependent of the split-K GEMM: wait for its
-  // end (and its partials) here, after this grid's launch overlapped it
+  // end (and its partials) here, after this grid's launch overlapped it.
+  // The next grid on the stream may be scheduled at once (it waits for
+  // this one's end before touching memory this one writes).
+  ptx::griddep_launch_dependents();
   ptx::griddep_wait();
   const size_t nvec = n / 8;
   const size_t stride = size_t(gridDim.x) * kThreads;

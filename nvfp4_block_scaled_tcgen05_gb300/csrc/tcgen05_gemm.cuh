@@ -572,6 +572,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (p.sk) {
       ptx::prefetch_tmap(&tmap_sfa);  // the stream-K workspace
     }
+    {
+      // The operand tiles of this CTA's first stages are pulled into L2
+      // while the previous grid on the stream finishes.  A prefetch moves
+      // no data into the CTA, so it may come before griddepcontrol.wait;
+      // the loads that follow it read the coherent L2 whatever the
+      // previous grid wrote.
+      Seg s0;
+      if (seg_at<Cfg>(p, cluster_id, num_clusters, 0, s0)) {
+        int l, mb, nb;
+        decode_tile<Cfg>(s0.tile, p, l, mb, nb);
+        if (p.k_splits > 1) l = l / p.k_splits;
+        const int a_row = mb * Cfg::TILE_M + int(peer) * Cfg::BM;
+        const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
+        const int kend = min(s0.kb1, s0.kb0 + STAGES);
+        for (int kb = s0.kb0; kb < kend; ++kb) {
+#pragma unroll
+          for (int sub = 0; sub < Cfg::KSUB; ++sub) {
+            const int x = kb * Cfg::KX * Cfg::KSUB + sub * Cfg::KX;
+            ptx::tma_prefetch_3d(&tmap_a, x, a_row, l);
+            if constexpr (!Cfg::kW4 && !Cfg::B_MN) ptx::tma_prefetch_3d(&tmap_b, x, b_row, l);
+          }
+          if constexpr (kFP4 && Cfg::SFA_REP)
+            ptx::tma_prefetch_3d(&tmap_sfa, 0, 0,
+                                 (l * p.rest_m + mb * CG + int(peer)) * p.rest_k + 4 * kb);
+        }
+      }
+    }
     // The next grid on the stream (the split-K reduce, the stream-K fixup,
     // or the next GEMM) may be scheduled now: it waits for this grid's end
     // before it touches global memory.
