@@ -560,6 +560,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
+  // The producer's first segment, found before the dependency wait: the
+  // schedule arithmetic run for the first time cost ~0.7 us between the
+  // wait and the first load.
+  Seg s0{};
+  int l0 = 0, mb0 = 0, nb0 = 0;
+  bool has0 = false;
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
@@ -578,13 +584,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // no data into the CTA, so it may come before griddepcontrol.wait;
       // the loads that follow it read the coherent L2 whatever the
       // previous grid wrote.
-      Seg s0;
-      if (seg_at<Cfg>(p, cluster_id, num_clusters, 0, s0)) {
-        int l, mb, nb;
-        decode_tile<Cfg>(s0.tile, p, l, mb, nb);
-        if (p.k_splits > 1) l = l / p.k_splits;
-        const int a_row = mb * Cfg::TILE_M + int(peer) * Cfg::BM;
-        const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
+      has0 = seg_at<Cfg>(p, cluster_id, num_clusters, 0, s0);
+      if (has0) {
+        decode_tile<Cfg>(s0.tile, p, l0, mb0, nb0);
+        const int l = (p.k_splits > 1) ? l0 / p.k_splits : l0;
+        const int a_row = mb0 * Cfg::TILE_M + int(peer) * Cfg::BM;
+        const int b_row = nb0 * BN + int(peer) * Cfg::B_ROWS;
         const int kend = min(s0.kb1, s0.kb0 + STAGES);
         for (int kb = s0.kb0; kb < kend; ++kb) {
 #pragma unroll
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
           if constexpr (kFP4 && Cfg::SFA_REP)
             ptx::tma_prefetch_3d(&tmap_sfa, 0, 0,
-                                 (l * p.rest_m + mb * CG + int(peer)) * p.rest_k + 4 * kb);
+                                 (l * p.rest_m + mb0 * CG + int(peer)) * p.rest_k + 4 * kb);
         }
       }
     }
@@ -666,9 +671,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       uint32_t armed = 0, armed_parity = 0;  // bit s: stage s has a load in flight / its parity
       bool ok = true;
       Seg sg;
-      for (int idx = 0; ok && seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg); ++idx) {
+      for (int idx = 0; ok; ++idx) {
         int l, mb, nb;
-        decode_tile<Cfg>(sg.tile, p, l, mb, nb);
+        if (idx == 0) {
+          if (!has0) break;
+          sg = s0;
+          l = l0;
+          mb = mb0;
+          nb = nb0;
+        } else {
+          if (!seg_at<Cfg>(p, cluster_id, num_clusters, idx, sg)) break;
+          decode_tile<Cfg>(sg.tile, p, l, mb, nb);
+        }
         const int a_row = mb * Cfg::TILE_M + int(peer) * Cfg::BM;
         const int b_row = nb * BN + int(peer) * Cfg::B_ROWS;
         int sfb_atoms = 0;

@@ -190,3 +190,71 @@ def test_splitk_workspace_is_not_read(g):
                                M, N, K, 4, workspace=ws)
     ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, 1, M, N, K)
     check_close16(bits16(c).reshape(M, N), ref, K, MAXDQ, MAXDQ, "f16", "stale workspace")
+
+
+@pytest.mark.parametrize("fill", [0x00, 0x7F, 0xFF])
+def test_splitk_any_workspace_contents_same_result(g, fill):
+    # batched decode-like split-K: whatever the workspace holds on entry, the
+    # result equals the one from a fresh workspace bit for bit
+    L, M, N, K = 2, 128, 512, 2048
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 171))
+    args = [to_dev_u8(x) for x in (a, b, sfa, sfb)]
+    need = L * g.gemm_nvfp4_bs_splitk_workspace_bytes(M, N, K, 4)
+    ws = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+    got = bits16(g.gemm_nvfp4_bs_splitk(*args, M, N, K, 4, workspace=ws, L=L)).reshape(L * M, N)
+    fresh = bits16(g.gemm_nvfp4_bs_splitk(*args, M, N, K, 4, L=L)).reshape(L * M, N)
+    assert np.array_equal(got, fresh)
+    ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K)
+    check_close16(got, ref, K, MAXDQ, MAXDQ, "f16", f"workspace fill {fill:#x}")
+
+
+def test_splitk_graph_replay(g):
+    # the GEMM and its reduce captured in one graph and replayed with new
+    # activations each time
+    M, N, K, S = 128, 768, 4096, 4
+    a, b, sfa, sfb = synth.nvfp4_inputs(synth.Nvfp4("t", 1, M, N, K, 181))
+    ad, bd, sad, sbd = [to_dev_u8(x) for x in (a, b, sfa, sfb)]
+    need = g.gemm_nvfp4_bs_splitk_workspace_bytes(M, N, K, S)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    c = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g.gemm_nvfp4_bs_splitk(ad, bd, sad, sbd, M, N, K, S, workspace=ws, c=c, stream=s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.gemm_nvfp4_bs_splitk(ad, bd, sad, sbd, M, N, K, S, workspace=ws, c=c, stream=s)
+    for seed in (182, 183, 184):
+        a2 = synth.nvfp4_inputs(synth.Nvfp4("t", 1, M, N, K, seed))[0]
+        ad.copy_(to_dev_u8(a2))
+        c.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle.gemm_nvfp4_bs(a2, b, sfa, sfb, 1, M, N, K)
+        check_close16(bits16(c).reshape(M, N), ref, K, MAXDQ, MAXDQ, "f16", f"replay {seed}")
+
+
+def test_splitk_back_to_back_shares_workspace(g):
+    # launches of different shapes and split counts queued on one stream
+    # without synchronisation, sharing one workspace (each GEMM's partials
+    # are read by its own reduce before the next GEMM writes them)
+    cases = [(1, 128, 512, 2048, 4), (2, 256, 256, 1024, 2), (1, 128, 768, 4096, 3)]
+    need = max(L * g.gemm_nvfp4_bs_splitk_workspace_bytes(M, N, K, S) for L, M, N, K, S in cases)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    inputs = [synth.nvfp4_inputs(synth.Nvfp4("t", L, M, N, K, 191 + i))
+              for i, (L, M, N, K, S) in enumerate(cases)]
+    devs = [[to_dev_u8(x) for x in inp] for inp in inputs]
+    outs = []
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for (L, M, N, K, S), d in zip(cases, devs):
+            outs.append(g.gemm_nvfp4_bs_splitk(*d, M, N, K, S, workspace=ws, L=L))
+    torch.cuda.synchronize()
+    for i, (L, M, N, K, S) in enumerate(cases):
+        a, b, sfa, sfb = inputs[i]
+        ref = oracle.gemm_nvfp4_bs(a, b, sfa, sfb, L, M, N, K)
+        first = bits16(outs[i]).reshape(L * M, N)
+        check_close16(first, ref, K, MAXDQ, MAXDQ, "f16", f"back to back {L}x{M}x{N}x{K}/{S}")
+        for rep in (1, 2):
+            assert np.array_equal(bits16(outs[rep * len(cases) + i]).reshape(L * M, N), first)
