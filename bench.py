@@ -737,7 +737,9 @@ def measure_lora(torch, lib, synth, up, stream, dev, pk, warmup, reps, check):
 
 
 def measure_router(torch, lib, synth, up, stream, dev, warmup, reps, check):
-    """Ordered router GEMM on CUDA cores (no-FMA FP32: 1 flop per lane per clock)."""
+    """Ordered router GEMM on CUDA cores: 2 flops per (multiply, add) pair,
+    against the FP32 pipe's one fused multiply-add (2 flops) per lane per
+    clock, which the kernel issues where the products are exact."""
     sp = stream.cuda_stream
     w = synth.ROUTER
     A_h, B_h = synth.gemm_inputs(w)
@@ -750,7 +752,7 @@ def measure_router(torch, lib, synth, up, stream, dev, warmup, reps, check):
                                                   Cr[i].data_ptr(), w.M, w.N, w.K, sp))
     sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
     props = torch.cuda.get_device_properties(dev)
-    alu_peak = props.multi_processor_count * 128 * 2070e6 / 1e12  # TFLOP/s at max SM clock
+    alu_peak = props.multi_processor_count * 128 * 2 * 2070e6 / 1e12  # FMA TFLOP/s, max SM clock
     tf = 2.0 * w.M * w.N * w.K / sec / 1e12
     res = {"shape": "router", "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
            "frac_alu_peak": tf / alu_peak, "alu_peak_tflops": alu_peak}
