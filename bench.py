@@ -440,7 +440,9 @@ def main():
     # row chunks of A/C (each chunk one gemm_bf16_nt call on 256-row-aligned
     # rows, so results equal the one-call GEMM bit for bit): host-to-device
     # copies, GEMMs and device-to-host copies run on three streams, and two
-    # device buffer sets let step i+1's copies proceed while step i drains.
+    # device buffer sets let step i+1's copies and GEMMs proceed while step
+    # i's result is still being read back.  The timed region runs the steps
+    # back to back and ends after the last step's read-back.
     A_pin = torch.from_numpy(A_h.view(np.int16)).pin_memory()
     B_pin = torch.from_numpy(B_h.view(np.int16)).pin_memory()
     C_pin = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
@@ -505,15 +507,39 @@ def main():
                     ev = torch.cuda.Event()
                     ev.record(sd)
                     ends.append(ev)
-        for ev in ends:
-            stream.wait_event(ev)  # the timing events on `stream` see the whole step
+        # one event for "C of this set has been read back"; the compute
+        # stream waits on it only before it next writes this set, so step
+        # i+1's GEMMs overlap step i's device-to-host copies
+        s0 = s_d2hs[0]
+        for ev in ends[1:]:
+            s0.wait_event(ev)
         done = torch.cuda.Event()
-        done.record(stream)
+        done.record(s0)
         done_d2h[j] = done
+        last_d2h[0] = done
+
+    last_d2h = [None]
+
+    def e2e_timed(nsteps):
+        """nsteps pipelined steps, timed on `stream` from before the first
+        copy to after the last step's device-to-host copies."""
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for s_ in s_h2ds + s_d2hs:
+            s_.wait_event(start)
+        for i in range(nsteps):
+            e2e_step(i)
+        stream.wait_event(last_d2h[0])
+        end.record(stream)
+        end.synchronize()
+        return start.elapsed_time(end) / 1e3 / nsteps
 
     e2e_steps = max(3, min(args.steps, 20))
-    e2e_sec, _ = time_launches(torch, stream, e2e_step, 1, 2, e2e_steps)
-    e2e_sec = max_over_ranks(e2e_sec)
+    for i in range(2):  # warm-up steps
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_sec = max_over_ranks(e2e_timed(e2e_steps))
     h2d = (w.M * w.K + w.N * w.K) * 2
     d2h = w.M * w.N * 2
     # the e2e output must equal the device-resident result bit for bit
