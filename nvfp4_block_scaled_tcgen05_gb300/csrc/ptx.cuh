@@ -127,17 +127,6 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
       : "memory");
 }
 
-// Plain (non-tensor) bulk copy global -> shared, completing on an mbarrier.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -145,11 +134,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- clusters
@@ -318,16 +302,6 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sd
                  : "memory");
 }
 
-// Copy a 128-row x 16-byte matrix from shared memory into TMEM lanes
-// 0..127 (row r -> lane r), 4 consecutive columns, no replication.
-template <int CG>
-__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-  if constexpr (CG == 1)
-    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-  else
-    asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Copy a 128-row x 32-byte matrix into TMEM lanes 0..127, 8 consecutive columns.
 template <int CG>
 __device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
@@ -335,10 +309,6 @@ __device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
   else
     asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base+t),

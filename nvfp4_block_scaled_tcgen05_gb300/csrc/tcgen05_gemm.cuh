@@ -1285,7 +1285,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           // then one TMA store per 32 columns; the tensor map clips rows
           // and weights past the output.  Scattered 4-byte stores of the
           // same data took about 4 us per 128 x 128 tile.
-          uint8_t* box = smem + (buf0 - sbase);
+          // The CTA's last tile (a decode CTA's only one): its MMAs, and so
+          // every use of the stages, are complete, so each box takes a
+          // place of its own in the stage memory and the stores go out
+          // without waiting for the previous box to be read.
+          constexpr uint32_t kBoxBytes = 32 * 32 * 4;
+          static_assert(Cfg::EPI_WARPS * (Cfg::EPI_COLS / 32) * kBoxBytes <=
+                            Cfg::STAGES * Cfg::STAGE_BYTES,
+                        "the last tile's boxes fit the stage memory");
+          Seg nx;
+          const bool last_tile = !seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, nx);
 #pragma unroll 1
           for (int c = 0; c < Cfg::EPI_COLS / 32; ++c) {
             uint32_t r0[32];
@@ -1294,8 +1303,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (c == Cfg::EPI_COLS / 32 - 1) release_acc(acc);
             const int j0 = nb * BN + col_base + 32 * c;  // activation row of r0[0]
             if (!rows_live || j0 >= p.N) continue;       // warp-uniform
-            if (lane == 0) ptx::bulk_wait_group_read<0>();  // the box's previous store read it
-            __syncwarp();
+            uint32_t bsm = buf0;
+            if (last_tile) {
+              bsm = sbase + uint32_t(e * (Cfg::EPI_COLS / 32) + c) * kBoxBytes;
+            } else {
+              if (lane == 0) ptx::bulk_wait_group_read<0>();  // the box's previous store read it
+              __syncwarp();
+            }
+            uint8_t* box = smem + (bsm - sbase);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
               if constexpr (EPI == Epilogue::kStoreF32)
@@ -1307,7 +1322,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              ptx::tma_store_3d(&tmap_c, buf0, row0, j0, int(slot));
+              ptx::tma_store_3d(&tmap_c, bsm, row0, j0, int(slot));
               ptx::bulk_commit_group();
             }
           }
@@ -1511,15 +1526,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
         }
       } else {
+        // The CTA's last whole tile: its MMAs, and so every use of the
+        // stages, are complete, so (where they fit) each output box takes a
+        // place of its own in the stage memory and the stores go out
+        // without waiting for a buffer to be read.
+        constexpr bool kLastInStages =
+            EPI != Epilogue::kScaledAccBF16 &&
+            Cfg::EPI_WARPS * (Cfg::EPI_COLS / 64) * Cfg::EPI_BOX_BYTES <=
+                Cfg::STAGES * Cfg::STAGE_BYTES;
+        bool last_tile = false;
+        if constexpr (kLastInStages) {
+          Seg nx;
+          last_tile = sg.slot < 0 && !seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, nx);
+        }
 #pragma unroll 1
         for (int c = 0; c < Cfg::EPI_COLS / 64; ++c, ++chunk_ctr) {
           const int b = int(chunk_ctr % Cfg::EPI_BUFS);
-          const uint32_t sbuf = buf0 + b * Cfg::EPI_BOX_BYTES;
+          const uint32_t sbuf =
+              last_tile ? sbase + uint32_t(e * (Cfg::EPI_COLS / 64) + c) * Cfg::EPI_BOX_BYTES
+                        : buf0 + b * Cfg::EPI_BOX_BYTES;
           const int col0 = nb * BN + col_base + c * 64;
           const bool live = rows_live && col0 < p.N;
           // The TMA store that last read this buffer must be done with it.
-          if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
-          __syncwarp();
+          if (!last_tile) {
+            if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
+            __syncwarp();
+          }
           if constexpr (EPI == Epilogue::kScaledAccBF16) {
             if (live && lane == 0) {
               ptx::mbar_arrive_expect_tx(epi_bar(e, b), Cfg::EPI_BOX_BYTES);
