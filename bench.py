@@ -339,6 +339,32 @@ def tensor_rate(torch, dev, local, n_mma=8192):
     return rows
 
 
+def probe_fp4_mma_rate(torch, dev, n_mma=8192, reps=20):
+    """The block-scaled MMA's own rate on this GPU now: the issue-rate probe
+    (kind::mxf4nvf4 256x256x64 back to back from zeroed shared memory, no
+    scale copies or commits) on every CTA pair, TFLOP/s by CUDA events."""
+    import ctypes
+    from nvfp4_block_scaled_tcgen05_gb300 import build as _b
+    lib = ctypes.CDLL(_b.PROBE_LIB)
+    f = lib.probe_tensor_rate
+    f.argtypes = [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 2
+    out = torch.zeros(2 * pairs, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(2):
+        if f(1, 256, pairs, n_mma, 0, 0, 0, 0, out.data_ptr(), stream):
+            raise RuntimeError("probe_tensor_rate failed")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        f(1, 256, pairs, n_mma, 0, 0, 0, 0, out.data_ptr(), stream)
+    e1.record()
+    e1.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / reps
+    return pairs * n_mma * 2.0 * 256 * 256 * 64 / sec / 1e12
+
+
 # ----------------------------------------------------------------- our arm
 def main():
     args = parse()
@@ -802,6 +828,8 @@ def measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_p
     fn = lambda i: check(lib.gemm_nvfp4_bs(sets[i][0].data_ptr(), sets[i][1].data_ptr(),
                                            sets[i][2].data_ptr(), sets[i][3].data_ptr(),
                                            cs[i].data_ptr(), w.L, w.M, w.N, w.K, sp))
+    # the MMA's own rate, measured by the issue-rate probe just before
+    probe_rate = probe_fp4_mma_rate(torch, dev)
     sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
     flops = 2.0 * w.L * w.M * w.N * w.K
     tf = flops / sec / 1e12
@@ -810,7 +838,9 @@ def measure_nvfp4(torch, lib, synth, up, stream, dev, warmup, reps, check, fp4_p
            "TFLOP/s": tf, "frac_fp4_peak": tf / fp4_peak, "fp4_peak_tflops": fp4_peak,
            "fp4_peak_source": "measured bf16 burst x nominal fp4/bf16 ratio 15/2.25",
            "fp4_mma_rate_tflops": mma_rate,
-           "frac_fp4_mma_rate": tf / mma_rate}
+           "frac_fp4_mma_rate": tf / mma_rate,
+           "fp4_probe_mma_rate_tflops": probe_rate,
+           "frac_fp4_probe_mma_rate": tf / probe_rate}
     # The same launches back to back for ~0.5 s with the SM clock sampled:
     # real FP4 operands draw enough power for the power cap to lower the
     # clock, and the MMA rate scales with it.

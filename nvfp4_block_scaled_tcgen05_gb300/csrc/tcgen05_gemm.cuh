@@ -1367,18 +1367,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                   *reinterpret_cast<uint4*>(dst + 32 * i + 8 * j) =
                       epi_chunk<EPI>(&r[i][8 * j], make_uint4(0, 0, 0, 0), 0.0f);
           }
-        } else
+        } else {
+          // the CTA's last tile: each box in a place of its own in the freed
+          // stage memory, no waits (as in the other epilogues)
+          constexpr bool kLastInStages =
+              Cfg::EPI_WARPS * NCH * Cfg::EPI_BOX_BYTES <= Cfg::STAGES * Cfg::STAGE_BYTES;
+          bool last_tile = false;
+          if constexpr (kLastInStages) {
+            Seg nx;
+            last_tile = sg.slot < 0 && !seg_at<Cfg>(p, cluster_id, num_clusters, idx + 1, nx);
+          }
 #pragma unroll
         for (int c = 0; c < NCH; ++c, ++chunk_ctr) {
           const int b = int(chunk_ctr % Cfg::EPI_BUFS);
-          const uint32_t sbuf = buf0 + b * Cfg::EPI_BOX_BYTES;
+          const uint32_t sbuf =
+              last_tile ? sbase + uint32_t(e * NCH + c) * Cfg::EPI_BOX_BYTES
+                        : buf0 + b * Cfg::EPI_BOX_BYTES;
           const int col0 = nb * BN + col_base + c * 64;
           if (!(rows_live && col0 < p.N)) continue;
-          if (lane == 0) {
-            if constexpr (Cfg::EPI_BUFS == 1) ptx::bulk_wait_group_read<0>();
-            else ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
+          if (!last_tile) {
+            if (lane == 0) {
+              if constexpr (Cfg::EPI_BUFS == 1) ptx::bulk_wait_group_read<0>();
+              else ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
+            }
+            __syncwarp();
           }
-          __syncwarp();
           write_box_row<EPI>(smem + (sbuf - sbase) + lane * 128, lane, r[2 * c], r[2 * c + 1],
                              p.scale);
           ptx::fence_proxy_async_smem();
@@ -1387,6 +1400,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             store_box(sbuf, col0, row0, l);
             ptx::bulk_commit_group();
           }
+        }
         }
       } else if constexpr (kLookahead) {
         // Scaled-acc with look-ahead: the old output boxes of this tile were
