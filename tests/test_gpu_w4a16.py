@@ -49,6 +49,7 @@ def amax(x):
     (129, 264, 512),     # one row / 8 columns past a tile
     (17, 1000, 2304),    # many stages, N not a multiple of 256
     (640, 768, 256),     # exact multiples
+    (1100, 1032, 768),   # five M blocks: the last work item's second tile lies past M
 ])
 def test_w4a16_ragged(g, M, N, K):
     w = synth.W4a16("t", M, N, K, 0.37, 300 + M)
