@@ -66,6 +66,17 @@ int current_device(DeviceInfo* out, void* stream) {
     cudaGetLastError();
     return GEMM_ERR_NO_DEVICE;
   }
+  // A host thread that has made no CUDA runtime call of its own has no
+  // current context, and the driver's tensor-map encoder needs one: bind
+  // the device's primary context to the calling thread once per device.
+  thread_local uint64_t bound_devices = 0;
+  if (!(bound_devices & (1ull << dev))) {
+    if (cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_DEVICE;
+    }
+    bound_devices |= 1ull << dev;
+  }
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceSlot& s = g_devices[dev];
   if (!s.ready) {
