@@ -18,6 +18,13 @@
  * stream capture; during a capture it returns GEMM_ERR_CAPTURE and does
  * nothing (a later call outside capture does the set-up).
  *
+ * Threads: any host thread may call any entry point, concurrently with
+ * others (the per-device set-up is serialised inside the library).  A
+ * thread's first call on a device makes that device's primary context
+ * current in the thread (cudaSetDevice on the device that is already
+ * current), because the driver's tensor-map encoder needs a current
+ * context; the current device is never changed.
+ *
  * Device-side wait limits: every wait inside a kernel is bounded (two
  * seconds).  A kernel that runs out of a wait stops, records a code in a
  * device status word and returns; gemm_get_device_status() reports it.
