@@ -1,7 +1,8 @@
 """Every output element of the full-size problems against the oracle (the
 other full-size tests sample rows): the BF16 GEMMs at gate/up, down, qkv and
-gqa through the default entry point, the NVFP4 decode shapes through
-split-K, and W4A16 at qkvz (~30 s of oracle on 16 host cores).  The NVFP4
+gqa through the default entry point, gate/up in the NN layout, down and qkv
+through stream-K, gqa through split-K, the NVFP4 decode shapes through
+split-K, and W4A16 at qkvz (~45 s of oracle on 16 host cores).  The NVFP4
 GEMM at 4096 x 7168 x 16384 takes the oracle ~5 minutes and runs only with
 --slow-oracle (its rows are sampled in the NVFP4 tests)."""
 from __future__ import annotations
@@ -54,6 +55,35 @@ def test_bf16_every_output(g, name):
     got = bits16(g.gemm_bf16_nt(to_dev_bf16(A), to_dev_bf16(B)))
     ref = oracle.gemm_bf16_nt(A, B)
     stats = check_all(got, ref, w.K, amax(A), amax(B), "bf16", name)
+    assert stats["frac_exact"] > 0.9, stats
+
+
+def test_bf16_nn_gateup_every_output(g):
+    # B stored [K][N]: the oracle takes it back to [N][K]
+    w = synth.BF16_WORKLOADS["gateup"]
+    A, B = synth.gemm_inputs(w)
+    Bt = np.ascontiguousarray(B.T)
+    got = bits16(g.gemm_bf16_nn(to_dev_bf16(A), to_dev_bf16(Bt)))
+    stats = check_all(got, oracle.gemm_bf16_nt(A, B), w.K, amax(A), amax(B), "bf16", "nn gateup")
+    assert stats["frac_exact"] > 0.9, stats
+
+
+@pytest.mark.parametrize("name", ["down", "qkv"])
+def test_bf16_streamk_every_output(g, name):
+    w = synth.BF16_WORKLOADS[name]
+    A, B = synth.gemm_inputs(w)
+    got = bits16(g.gemm_bf16_nt_streamk(to_dev_bf16(A), to_dev_bf16(B)))
+    stats = check_all(got, oracle.gemm_bf16_nt(A, B), w.K, amax(A), amax(B), "bf16",
+                      f"{name} stream-K")
+    assert stats["frac_exact"] > 0.9, stats
+
+
+def test_bf16_splitk_gqa_every_output(g):
+    w = synth.BF16_WORKLOADS["gqa"]
+    A, B = synth.gemm_inputs(w)
+    got = bits16(g.gemm_bf16_nt_splitk(to_dev_bf16(A), to_dev_bf16(B), 4))
+    stats = check_all(got, oracle.gemm_bf16_nt(A, B), w.K, amax(A), amax(B), "bf16",
+                      "gqa split-K 4")
     assert stats["frac_exact"] > 0.9, stats
 
 
