@@ -19,11 +19,12 @@
  * nothing (a later call outside capture does the set-up).
  *
  * Threads: any host thread may call any entry point, concurrently with
- * others (the per-device set-up is serialised inside the library).  A
- * thread's first call on a device makes that device's primary context
- * current in the thread (cudaSetDevice on the device that is already
- * current), because the driver's tensor-map encoder needs a current
- * context; the current device is never changed.
+ * others (the per-device set-up is serialised inside the library).  The
+ * driver's tensor-map encoder needs a current context: a call from a thread
+ * that has none makes the current device's primary context current there
+ * (cudaSetDevice on the device that is already current).  A context the
+ * caller made current is left as it is, and the current device is never
+ * changed.
  *
  * Device-side wait limits: every wait inside a kernel is bounded (two
  * seconds).  A kernel that runs out of a wait stops, records a code in a

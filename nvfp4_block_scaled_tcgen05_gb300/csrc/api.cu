@@ -48,6 +48,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // [a, a+na) and [b, b+nb) overlap?
@@ -67,15 +83,17 @@ int current_device(DeviceInfo* out, void* stream) {
     return GEMM_ERR_NO_DEVICE;
   }
   // A host thread that has made no CUDA runtime call of its own has no
-  // current context, and the driver's tensor-map encoder needs one: bind
-  // the device's primary context to the calling thread once per device.
-  thread_local uint64_t bound_devices = 0;
-  if (!(bound_devices & (1ull << dev))) {
-    if (cudaSetDevice(dev) != cudaSuccess) {
+  // current context, and the driver's tensor-map encoder needs one: then
+  // make the device's primary context current in this thread.  A context
+  // the caller made current (primary or not) is left as it is.
+  {
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    const CUresult r = get ? get(&ctx) : CUDA_ERROR_NOT_INITIALIZED;
+    if ((r != CUDA_SUCCESS || ctx == nullptr) && cudaSetDevice(dev) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_NO_DEVICE;
     }
-    bound_devices |= 1ull << dev;
   }
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceSlot& s = g_devices[dev];
