@@ -894,12 +894,26 @@ def measure_w4a16(torch, lib, synth, up, stream, dev, warmup, reps, check, bf16_
                                             ws.data_ptr(), ctypes.c_size_t(ws_bytes),
                                             w.M, w.N, w.K, sp))
     sec2, _ = time_launches(torch, stream, fn2, n, warmup, reps)
+    # the same weights in the transposed layout (codes [K/2][ldb], scales
+    # [K/16][ldb], ldb = N rounded up to 128)
+    ldb = -(-w.N // 128) * 128
+    bt_h = np.zeros((w.K // 2, ldb), dtype=np.uint8)
+    st_h = np.zeros((w.K // 16, ldb), dtype=np.uint8)
+    bt_h[:, :w.N] = b_h.T
+    st_h[:, :w.N] = sfb_h.T
+    bt0, st0 = up(bt_h), up(st_h)
+    tsets = [(sets[0][0], bt0, st0)] + [(sets[i][0], bt0.clone(), st0.clone()) for i in range(1, n)]
+    fn3 = lambda i: check(lib.gemm_w4a16_t(tsets[i][0].data_ptr(), tsets[i][1].data_ptr(),
+                                           tsets[i][2].data_ptr(), scale2, cs[i].data_ptr(),
+                                           w.M, w.N, w.K, ldb, sp))
+    sec3, _ = time_launches(torch, stream, fn3, n, warmup, reps)
     tf = 2.0 * w.M * w.N * w.K / sec / 1e12
-    del sets, cs, ws
+    del sets, tsets, cs, ws
     return {"shape": name, "M": w.M, "N": w.N, "K": w.K, "us": sec * 1e6, "TFLOP/s": tf,
             "frac_bf16_peak": tf / bf16_peak,
             "weight_bytes": int(b_h.size + sfb_h.size),
-            "two_pass_us": sec2 * 1e6}
+            "two_pass_us": sec2 * 1e6,
+            "transposed_layout_us": sec3 * 1e6}
 
 
 def measure_nvfp4_decode(torch, lib, synth, up, stream, dev, pk, warmup, reps, check, fp4_peak,
