@@ -57,8 +57,10 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            # ORACLE_LIB names another build of oracle.c to load instead (the
+            # planted-mistake tests load deliberately broken copies this way)
+            path = os.environ.get("ORACLE_LIB") or build()
+            lib = ctypes.CDLL(path)
             u16p = ctypes.POINTER(ctypes.c_uint16)
             u8p = ctypes.POINTER(ctypes.c_uint8)
             f32p = ctypes.POINTER(ctypes.c_float)
