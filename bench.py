@@ -935,11 +935,30 @@ def measure_nvfp4_decode(torch, lib, synth, up, stream, dev, pk, warmup, reps, c
         sets[i][0].data_ptr(), sets[i][1].data_ptr(), sets[i][2].data_ptr(), sets[i][3].data_ptr(),
         cs[i].data_ptr(), ws.data_ptr(), ws_bytes, 1, w.M, w.N, w.K, k_splits, sp))
     sec, _ = time_launches(torch, stream, fn, n, warmup, reps)
+    # the same calls replayed from one CUDA graph, the way a decode loop runs
+    # them (the launch gaps of the host are gone; the kernels and their
+    # programmatic dependent launches are the same)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(reps):
+            fn(i % n)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        graph.replay()
+        stream.synchronize()
+        g0.record(stream)
+        graph.replay()
+        g1.record(stream)
+    g1.synchronize()
+    gsec = g0.elapsed_time(g1) / 1e3 / reps
+    del graph
     tf = 2.0 * w.M * w.N * w.K / sec / 1e12
     gbs = set_bytes / sec / 1e9
     res = {"shape": name, "L": 1, "M": w.M, "N": w.N, "K": w.K, "k_splits": k_splits,
            "us": sec * 1e6, "TFLOP/s": tf, "frac_fp4_peak": tf / fp4_peak,
            "GB/s": gbs, "frac_hbm_peak": gbs / pk["hbm_gbs"],
+           "graph_us": gsec * 1e6, "graph_frac_hbm_peak": set_bytes / gsec / 1e9 / pk["hbm_gbs"],
            "bytes": int(set_bytes), "note": "operands + scales + fp16 output; split-K workspace "
            "traffic (L2-resident) not counted"}
     del sets, cs, ws
